@@ -1,0 +1,260 @@
+// Host side of the C ABI declared in include/kda.h: argument validation,
+// workspace layout, and the K0 -> K1 -> K2 launch sequence on one stream.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/kda.h"
+#include "kda_common.cuh"
+
+namespace kda {
+cudaError_t launch_varlen_schedule(const Problem &p, cudaStream_t stream);
+cudaError_t launch_prep(const Problem &p, cudaStream_t stream);
+cudaError_t launch_recur(const Problem &p, cudaStream_t stream);
+}  // namespace kda
+
+// Sticky per-device data-error word (KDA_DEVICE_* codes).
+static __device__ int g_kda_device_status = 0;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kMatBytes = 2ull * kda::kChunk * kda::kChunk * sizeof(__half);  // 16 KiB
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t flag_off, chunk_off_off, order_off, mats_off, total;
+};
+
+bool sizes_ok(int B, int T, int H, int K, int V, int N) {
+  return B >= 1 && T >= 0 && H >= 1 && K >= 1 && V >= 1 && N >= 0;
+}
+
+int64_t max_chunks_of(int B, int T, int N) {
+  return (int64_t)B * ((T + kda::kChunk - 1) / kda::kChunk) + (int64_t)N;
+}
+
+Layout layout_of(int B, int T, int H, int N) {
+  Layout L;
+  size_t off = 0;
+  L.flag_off = off;
+  off = align_up(off + sizeof(int32_t));
+  L.chunk_off_off = off;
+  off = align_up(off + sizeof(int32_t) * ((size_t)N + 1));
+  L.order_off = off;
+  off = align_up(off + sizeof(int32_t) * ((size_t)N + 1));
+  L.mats_off = off;
+  off = align_up(off + (size_t)max_chunks_of(B, T, N) * (size_t)H * kMatBytes);
+  L.total = off;
+  return L;
+}
+
+bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+kda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+// Shared argument checks of kda_fwd and kda_debug_chunk_matrices.
+kda_status_t check_common(const void *q, const void *k, const void *g, const void *beta,
+                          const float *A_log, const float *dt_bias, float lower_bound,
+                          const int32_t *cu_seqlens, int B, int T, int H, int K, int num_seqs) {
+  if (!sizes_ok(B, T, H, K, K, num_seqs)) return KDA_ERR_INVALID_ARG;
+  // token tensors may be null only when they hold no elements (T == 0)
+  if (!A_log || (T > 0 && (!q || !k || !g || !beta))) return KDA_ERR_INVALID_ARG;
+  if (K != 64 && K != 128) return KDA_ERR_UNSUPPORTED;
+  if (!std::isfinite(lower_bound) || lower_bound < -5.0f || lower_bound > 0.0f) return KDA_ERR_INVALID_ARG;
+  if (cu_seqlens) {
+    if (B != 1) return KDA_ERR_INVALID_ARG;
+    if (!aligned(cu_seqlens, 4)) return KDA_ERR_INVALID_ARG;
+  } else if (num_seqs != B) {
+    return KDA_ERR_INVALID_ARG;
+  }
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(g, 16) || !aligned(beta, 2) ||
+      !aligned(A_log, 4) || (dt_bias && !aligned(dt_bias, 4)))
+    return KDA_ERR_INVALID_ARG;
+  // element counts must fit the 64-bit index arithmetic of the kernels
+  const double elems = (double)B * (double)T * (double)H * (double)K;
+  if (elems > 9.0e15) return KDA_ERR_INVALID_ARG;
+  if ((double)max_chunks_of(B, T, num_seqs) * H > 2.0e9) return KDA_ERR_UNSUPPORTED;
+  return KDA_OK;
+}
+
+struct Scratch {
+  void *ptr = nullptr;
+  bool owned = false;
+};
+
+kda_status_t get_scratch(void *workspace, size_t workspace_bytes, size_t need, cudaStream_t stream,
+                         Scratch &out) {
+  if (workspace) {
+    if (workspace_bytes < need || !aligned(workspace, kAlign)) return KDA_ERR_WORKSPACE;
+    out.ptr = workspace;
+    out.owned = false;
+    return KDA_OK;
+  }
+  if (cudaMallocAsync(&out.ptr, need, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_WORKSPACE;
+  }
+  out.owned = true;
+  return KDA_OK;
+}
+
+void release_scratch(Scratch &s, cudaStream_t stream) {
+  if (s.owned && s.ptr) cudaFreeAsync(s.ptr, stream);
+  s.ptr = nullptr;
+}
+
+kda_status_t fill_problem(kda::Problem &p, const Layout &L, void *ws, const void *q, const void *k,
+                          const void *v, const void *g, const void *beta, const float *A_log,
+                          const float *dt_bias, float lower_bound, float scale,
+                          const float *initial_state, float *final_state, const int32_t *cu,
+                          int B, int T, int H, int K, int V, int N, void *o) {
+  std::memset(&p, 0, sizeof p);
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.k = static_cast<const __nv_bfloat16 *>(k);
+  p.v = static_cast<const __nv_bfloat16 *>(v);
+  p.g = static_cast<const __nv_bfloat16 *>(g);
+  p.beta = static_cast<const __nv_bfloat16 *>(beta);
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.init = initial_state;
+  p.final_state = final_state;
+  p.cu = cu;
+  p.o = static_cast<__nv_bfloat16 *>(o);
+  char *base = static_cast<char *>(ws);
+  p.flag = cu ? reinterpret_cast<int32_t *>(base + L.flag_off) : nullptr;
+  p.chunk_off = reinterpret_cast<int32_t *>(base + L.chunk_off_off);
+  p.order = reinterpret_cast<int32_t *>(base + L.order_off);
+  p.mats = reinterpret_cast<__half *>(base + L.mats_off);
+  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p.dev_status), g_kda_device_status) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  p.lb = lower_bound;
+  p.scale = scale;
+  p.B = B;
+  p.T = T;
+  p.H = H;
+  p.K = K;
+  p.V = V;
+  p.N = N;
+  p.nc_fixed = (T + kda::kChunk - 1) / kda::kChunk;
+  p.max_chunks = cu ? max_chunks_of(1, T, N) : (long long)B * p.nc_fixed;
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_version(void) { return 100; }
+
+int64_t kda_max_chunks(int B, int T, int num_seqs) {
+  if (B < 1 || T < 0 || num_seqs < 0) return 0;
+  return max_chunks_of(B, T, num_seqs);
+}
+
+size_t kda_fwd_workspace_size(int B, int T, int H, int K, int V, int num_seqs) {
+  if (!sizes_ok(B, T, H, K, V, num_seqs)) return 0;
+  return layout_of(B, T, H, num_seqs).total;
+}
+
+const char *kda_status_string(kda_status_t s) {
+  switch (s) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported head dimension or size";
+    case KDA_ERR_WORKSPACE: return "workspace too small, misaligned, or allocation failed";
+    case KDA_ERR_CUDA: return "CUDA runtime error";
+    case KDA_ERR_DEVICE_STATUS: return "device reported a data error";
+  }
+  return "unknown status";
+}
+
+kda_status_t kda_get_device_status(kda_stream_t stream, int *device_code) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KDA_ERR_CUDA;
+  int code = 0;
+  if (cudaMemcpyFromSymbol(&code, g_kda_device_status, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_kda_device_status, &zero, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+  if (device_code) *device_code = code;
+  return code == 0 ? KDA_OK : KDA_ERR_DEVICE_STATUS;
+}
+
+kda_status_t kda_fwd_with_events(const void *q, const void *k, const void *v, const void *g,
+                                 const void *beta, const float *A_log, const float *dt_bias,
+                                 float lower_bound, float scale, const float *initial_state,
+                                 float *final_state, const int32_t *cu_seqlens, int B, int T, int H,
+                                 int K, int V, int num_seqs, void *o, void *workspace,
+                                 size_t workspace_bytes, kda_stream_t stream,
+                                 const kda_stage_events_t *events) {
+  kda_status_t st = check_common(q, k, g, beta, A_log, dt_bias, lower_bound, cu_seqlens, B, T, H, K,
+                                 num_seqs);
+  if (st != KDA_OK) return st;
+  if (V < 1) return KDA_ERR_INVALID_ARG;
+  if (T > 0 && (!v || !o)) return KDA_ERR_INVALID_ARG;
+  if (V != 64 && V != 128) return KDA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
+  if (!aligned(v, 16) || !aligned(o, 16) || (initial_state && !aligned(initial_state, 16)) ||
+      (final_state && !aligned(final_state, 16)))
+    return KDA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (num_seqs == 0) return KDA_OK;
+  const Layout L = layout_of(B, T, H, num_seqs);
+  Scratch scr;
+  st = get_scratch(workspace, workspace_bytes, L.total, s, scr);
+  if (st != KDA_OK) return st;
+  kda::Problem p;
+  st = fill_problem(p, L, scr.ptr, q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
+                    final_state, cu_seqlens, B, T, H, K, V, num_seqs, o);
+  auto mark = [&](void *ev) {
+    if (st == KDA_OK && ev) st = from_cuda(cudaEventRecord(static_cast<cudaEvent_t>(ev), s));
+  };
+  mark(events ? events->prep_start : nullptr);
+  if (st == KDA_OK && cu_seqlens) st = from_cuda(kda::launch_varlen_schedule(p, s));
+  if (st == KDA_OK) st = from_cuda(kda::launch_prep(p, s));
+  mark(events ? events->prep_done : nullptr);
+  if (st == KDA_OK) st = from_cuda(kda::launch_recur(p, s));
+  mark(events ? events->recur_done : nullptr);
+  release_scratch(scr, s);
+  return st;
+}
+
+kda_status_t kda_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                     const float *A_log, const float *dt_bias, float lower_bound, float scale,
+                     const float *initial_state, float *final_state, const int32_t *cu_seqlens,
+                     int B, int T, int H, int K, int V, int num_seqs, void *o, void *workspace,
+                     size_t workspace_bytes, kda_stream_t stream) {
+  return kda_fwd_with_events(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
+                             final_state, cu_seqlens, B, T, H, K, V, num_seqs, o, workspace,
+                             workspace_bytes, stream, nullptr);
+}
+
+kda_status_t kda_debug_chunk_matrices(const void *q, const void *k, const void *g, const void *beta,
+                                      const float *A_log, const float *dt_bias, float lower_bound,
+                                      const int32_t *cu_seqlens, int B, int T, int H, int K,
+                                      int num_seqs, void *chunk_mats, void *workspace,
+                                      size_t workspace_bytes, kda_stream_t stream) {
+  kda_status_t st = check_common(q, k, g, beta, A_log, dt_bias, lower_bound, cu_seqlens, B, T, H, K,
+                                 num_seqs);
+  if (st != KDA_OK) return st;
+  if (!chunk_mats || !aligned(chunk_mats, 16)) return KDA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (num_seqs == 0) return KDA_OK;
+  const Layout L = layout_of(B, T, H, num_seqs);
+  Scratch scr;
+  st = get_scratch(workspace, workspace_bytes, L.total, s, scr);
+  if (st != KDA_OK) return st;
+  kda::Problem p;
+  st = fill_problem(p, L, scr.ptr, q, k, k, g, beta, A_log, dt_bias, lower_bound, 1.0f, nullptr, nullptr,
+                    cu_seqlens, B, T, H, K, K, num_seqs, nullptr);
+  p.mats = static_cast<__half *>(chunk_mats);
+  if (st == KDA_OK && cu_seqlens) st = from_cuda(kda::launch_varlen_schedule(p, s));
+  if (st == KDA_OK) st = from_cuda(kda::launch_prep(p, s));
+  release_scratch(scr, s);
+  return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// Shared device-side definitions of the KDA chunked forward (sm_103a).
+//
+// Everything here is plumbing used by several kernels: the problem descriptor,
+// the mapping from (sequence, chunk) to token rows, and a few hardware math
+// instructions (ex2.approx / rcp.approx are single PTX instructions of the SFU;
+// the FlashKDA page, section "저수준(Low-level) 명령어 및 메모리 활용", uses the
+// same base-2 exponential trick).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int kChunk = 64;          // tokens per chunk
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNormEps = 1e-6f;   // L2-norm epsilon inside the square root
+
+// Device data-error codes (mirrors KDA_DEVICE_* in include/kda.h).
+constexpr int kDevOk = 0;
+constexpr int kDevBadCuSeqlens = 1;
+constexpr int kDevWaitTimeout = 2;
+
+struct Problem {
+  const __nv_bfloat16 *q, *k, *v, *g, *beta;
+  const float *A_log, *dt_bias;      // dt_bias may be null
+  const float *init;                 // [N,H,V,K] or null
+  float *final_state;                // [N,H,V,K] or null
+  const int32_t *cu;                 // [N+1] or null (fixed length)
+  __nv_bfloat16 *o;                  // [B,T,H,V]
+  __half *mats;                      // [max_chunks][H][2C][C] fp16 hand-off
+  int32_t *chunk_off;                // [N+1] varlen chunk offsets (K0 output)
+  int32_t *order;                    // [N] varlen longest-first order (K0 output)
+  int32_t *flag;                     // per-call data-error flag (varlen) or null
+  int *dev_status;                   // sticky per-device status word
+  float lb, scale;
+  int B, T, H, K, V, N;
+  int nc_fixed;                      // ceil(T / C) in fixed-length mode
+  long long max_chunks;
+};
+
+struct SeqInfo {
+  int b;        // batch row
+  int t0;       // first token
+  int len;      // number of tokens
+  int chunk0;   // global chunk index of the first chunk
+};
+
+__device__ __forceinline__ SeqInfo seq_info(const Problem &p, int s) {
+  SeqInfo r;
+  if (p.cu) {
+    r.b = 0;
+    r.t0 = p.cu[s];
+    r.len = p.cu[s + 1] - r.t0;
+    r.chunk0 = p.chunk_off[s];
+  } else {
+    r.b = s;
+    r.t0 = 0;
+    r.len = p.T;
+    r.chunk0 = s * p.nc_fixed;
+  }
+  return r;
+}
+
+// Row index of token t of batch row b, head h in a [B,T,H,*] tensor.
+__device__ __forceinline__ long long tok_row(const Problem &p, int b, int t, int h) {
+  return ((long long)b * p.T + t) * p.H + h;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Logistic function from one base-2 exponential and one reciprocal.
+// Saturates correctly: x -> +inf gives 1, x -> -inf gives 0.
+__device__ __forceinline__ float sigmoid_fast(float x) {
+  return rcp_approx(1.0f + ex2_approx(-x * kLog2e));
+}
+
+// Per-token base-2 log decay:  log2(alpha) = lb * log2(e) * sigmoid(ea * (g + dt)).
+__device__ __forceinline__ float log2_decay(float g, float dt, float ea, float lb_log2e) {
+  return lb_log2e * sigmoid_fast(ea * (g + dt));
+}
+
+__device__ __forceinline__ float to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Global chunk index -> sequence (binary search over the varlen chunk offsets).
+__device__ __forceinline__ int chunk_to_seq(const Problem &p, long long c) {
+  if (!p.cu) return (int)(c / p.nc_fixed);
+  int lo = 0, hi = p.N;  // chunk_off[lo] <= c < chunk_off[hi]
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (p.chunk_off[mid] <= c) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+}  // namespace kda

@@ -1,0 +1,141 @@
+"""Python binding of the KDA chunked forward C ABI (argument marshalling only).
+
+``fwd`` mirrors the KDA forward call of the cuLA / FLA API (cuLA README mirror,
+"Quick Start"; FlashKDA page, "flash-linear-attention 백엔드로 사용"), with the
+in-kernel options fixed on: q/k L2 norm, gate activation with a lower bound,
+beta sigmoid, and the [N,H,V,K] state layout. All compute runs in libkda.so on
+the caller's current CUDA stream; torch only provides device memory.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import torch
+
+from ._lib import check, lib
+
+__all__ = ["fwd", "workspace_size", "debug_chunk_matrices", "device_status", "max_chunks"]
+
+
+class _StageEvents(ctypes.Structure):
+    _fields_ = [("prep_start", ctypes.c_void_p), ("prep_done", ctypes.c_void_p),
+                ("recur_done", ctypes.c_void_p)]
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def workspace_size(B: int, T: int, H: int, K: int, V: int, num_seqs: int) -> int:
+    return int(lib().kda_fwd_workspace_size(B, T, H, K, V, num_seqs))
+
+
+def max_chunks(B: int, T: int, num_seqs: int) -> int:
+    return int(lib().kda_max_chunks(B, T, num_seqs))
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+        A_log: torch.Tensor, dt_bias: Optional[torch.Tensor] = None, lower_bound: float = -5.0,
+        scale: Optional[float] = None, initial_state: Optional[torch.Tensor] = None,
+        output_final_state: bool = False, cu_seqlens: Optional[torch.Tensor] = None,
+        workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+        final_state: Optional[torch.Tensor] = None,
+        events=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """KDA chunked forward on the GPU.
+
+    q, k, g: bf16 [B,T,H,K]; v: bf16 [B,T,H,V]; beta: bf16 [B,T,H] logits;
+    A_log: fp32 [H]; dt_bias: fp32 [H,K] (or [H*K]) or None; initial_state:
+    fp32 [N,H,V,K] or None; cu_seqlens: int32 [N+1] or None (then B must be 1).
+    Returns (o bf16 [B,T,H,V], final_state fp32 [N,H,V,K] or None).
+    events: optional (prep_start, prep_done, recur_done) torch.cuda.Event triple
+    recorded on the current stream at the kernel boundaries (profiling only).
+    """
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, (B, T, H, K))
+    _need(g, "g", torch.bfloat16, (B, T, H, K))
+    _need(v, "v", torch.bfloat16, (B, T, H, V))
+    _need(beta, "beta", torch.bfloat16, (B, T, H))
+    _need(A_log, "A_log", torch.float32, (H,))
+    if dt_bias is not None:
+        _need(dt_bias, "dt_bias", torch.float32)
+        if dt_bias.numel() != H * K:
+            raise ValueError("dt_bias must hold H*K values")
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, (N, H, V, K))
+    if scale is None:
+        scale = K ** -0.5
+    dev = q.device
+    o = out if out is not None else torch.empty(B, T, H, V, dtype=torch.bfloat16, device=dev)
+    _need(o, "out", torch.bfloat16, (B, T, H, V))
+    fs = None
+    if output_final_state:
+        fs = final_state if final_state is not None else torch.empty(N, H, V, K, dtype=torch.float32,
+                                                                     device=dev)
+        _need(fs, "final_state", torch.float32, (N, H, V, K))
+    need = workspace_size(B, T, H, K, V, N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace too small: need {need} bytes")
+    ev = None
+    if events is not None:
+        ev = ctypes.byref(_StageEvents(*[ctypes.c_void_p(e.cuda_event if e is not None else 0)
+                                         for e in events]))
+    with torch.cuda.device(dev):
+        rc = lib().kda_fwd_with_events(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log),
+                                       _ptr(dt_bias), float(lower_bound), float(scale),
+                                       _ptr(initial_state), _ptr(fs), _ptr(cu_seqlens), B, T, H, K, V, N,
+                                       _ptr(o), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream_ptr(), ev)
+    check("kda_fwd", rc)
+    return o, fs
+
+
+def debug_chunk_matrices(q, k, g, beta, A_log, dt_bias=None, lower_bound=-5.0, cu_seqlens=None):
+    """The prep kernel's per-(chunk, head) hand-off matrices, fp16 [max_chunks, H, 128, 64]."""
+    B, T, H, K = q.shape
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    mc = max_chunks(B, T, N)
+    mats = torch.zeros(max(mc, 1), H, 128, 64, dtype=torch.float16, device=q.device)
+    ws = torch.empty(max(workspace_size(B, T, H, K, K, N), 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib().kda_debug_chunk_matrices(_ptr(q), _ptr(k), _ptr(g), _ptr(beta), _ptr(A_log),
+                                            _ptr(dt_bias), float(lower_bound), _ptr(cu_seqlens), B, T,
+                                            H, K, N, _ptr(mats), _ptr(ws), ws.numel(), _stream_ptr())
+    check("kda_debug_chunk_matrices", rc)
+    return mats[:mc]
+
+
+def device_status(stream=None) -> int:
+    """Synchronise and read+clear the device data-error word (0 = none)."""
+    code = ctypes.c_int(0)
+    rc = lib().kda_get_device_status(_stream_ptr(stream), ctypes.byref(code))
+    if rc not in (0, 5):
+        check("kda_get_device_status", rc)
+    return int(code.value)

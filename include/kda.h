@@ -1,0 +1,193 @@
+/*
+ * kda.h - C ABI of the GB300 (sm_103a) chunked forward pass of Kimi Delta
+ * Attention (KDA).
+ *
+ * The operation (Kimi Delta Attention, arXiv:2510.26692, the paper cited by
+ * the cuLA overview page on discuss.pytorch.kr, section "cuLA 소개"), per
+ * sequence s and head h, for tokens t in order:
+ *
+ *   log alpha_t[k] = lower_bound * sigmoid(exp(A_log[h]) * (g[t,h,k] + dt_bias[h,k]))
+ *   q_hat = q / sqrt(|q|^2 + 1e-6),  k_hat = k / sqrt(|k|^2 + 1e-6)
+ *   beta_t = sigmoid(beta_logit[t,h])
+ *   S_t = (I - beta_t k_hat k_hat^T) Diag(alpha_t) S_{t-1} + beta_t k_hat v_t^T   (S is K x V)
+ *   o_t = scale * S_t^T q_hat
+ *
+ * The argument list and layouts follow the flash_kda.fwd parameter table on
+ * the FlashKDA page (discuss.pytorch.kr, section "FlashKDA의 KDA 연산 구조"):
+ * q/k/g bf16 [B,T,H,K], v bf16 [B,T,H,V], beta bf16 [B,T,H] logits, A_log
+ * fp32 [H], dt_bias fp32 [H,K], lower_bound in [-5, 0], optional fp32
+ * initial/final state [B,H,V,K]; the gate activation, q/k L2 norm and beta
+ * sigmoid run inside the kernels (same section). Packed variable-length
+ * batches pass int32 cu_seqlens (cuLA README mirror on shadowgraph.io,
+ * "Quick Start" notes); then B must be 1 and the state has one row per
+ * sequence. The computation is chunked (64 tokens per chunk, as in the FLA
+ * and cuLA kernels described in section "Flash Linear Attention과 비교") and
+ * split into a token-parallel prep kernel and a head-parallel recurrence
+ * kernel (FlashKDA page, section "커널 퓨전(Kernel Fusion) 전략의 분리").
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are DEVICE pointers to contiguous row-major data,
+ *     except where stated. The caller owns every buffer; the library keeps no
+ *     pointer after a call returns. Work is enqueued on `stream` and is
+ *     asynchronous: results are ready when the stream is synchronised.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns a status and enqueues nothing.
+ *   - Errors found on the device (a malformed cu_seqlens) are recorded in a
+ *     per-device status word and the kernels of that call return early
+ *     without writing o; kda_get_device_status() reads and clears the word.
+ *   - Nothing throws or aborts across this boundary.
+ */
+#ifndef KDA_GB300_KDA_H_
+#define KDA_GB300_KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle (a cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad alignment, bad scalar */
+  KDA_ERR_UNSUPPORTED = 2,   /* head dims other than K, V in {64, 128} */
+  KDA_ERR_WORKSPACE = 3,     /* workspace too small, or allocating it failed */
+  KDA_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+  KDA_ERR_DEVICE_STATUS = 5  /* the device recorded a data error (see below) */
+} kda_status_t;
+
+/* Device-side error codes reported through kda_get_device_status(). */
+#define KDA_DEVICE_OK 0
+#define KDA_DEVICE_BAD_CU_SEQLENS 1   /* cu_seqlens[0] != 0, decreasing, or cu_seqlens[N] != T */
+#define KDA_DEVICE_WAIT_TIMEOUT 2     /* a bounded pipeline wait in a kernel gave up */
+
+/* Tokens per chunk of the chunked algorithm. */
+#define KDA_CHUNK 64
+
+/*
+ * Bytes of scratch memory kda_fwd() needs for a problem of this size.
+ * num_seqs is the number of sequences N: B without cu_seqlens, the length of
+ * cu_seqlens minus one with it. Returns 0 when the sizes are invalid.
+ * The scratch holds, per chunk and head, the 128 x 64 fp16 matrix
+ * [-(I+A)^{-1} diag(beta); P (I+A)^{-1} diag(beta)] that the prep kernel
+ * hands to the recurrence kernel, plus the varlen schedule.
+ */
+KDA_API size_t kda_fwd_workspace_size(int B, int T, int H, int K, int V, int num_seqs);
+
+/*
+ * KDA chunked forward.
+ *
+ *   q, k, g      bf16 [B,T,H,K]; g is the pre-activation gate.
+ *   v            bf16 [B,T,H,V].
+ *   beta         bf16 [B,T,H] logits (sigmoid applied inside).
+ *   A_log        fp32 [H].
+ *   dt_bias      fp32 [H,K], or NULL for zeros.
+ *   lower_bound  finite, in [-5, 0].
+ *   scale        finite output scale (usually K^-0.5).
+ *   initial_state fp32 [N,H,V,K] (state[s,h,v,k] = S[k,v]) or NULL for zeros.
+ *   final_state  fp32 [N,H,V,K] to receive the last state, or NULL. It may be
+ *                the same pointer as initial_state (in-place update); any
+ *                other overlap is not allowed.
+ *   cu_seqlens   int32 [N+1] prefix offsets of packed sequences, or NULL. When
+ *                set, B must be 1, T is the packed length, and N = num_seqs.
+ *                Zero-length sequences are allowed (their state is copied).
+ *   B, T, H, K, V  sizes; K and V in {64, 128}; T may be 0.
+ *   num_seqs     N: equal to B when cu_seqlens is NULL.
+ *   o            bf16 [B,T,H,V] output.
+ *   workspace    device scratch of at least kda_fwd_workspace_size() bytes,
+ *                256-byte aligned, or NULL to let the call allocate and free
+ *                it stream-ordered (cudaMallocAsync / cudaFreeAsync).
+ *   stream       the CUDA stream to enqueue on.
+ *
+ * Alignment: q, k, v, g, o, initial_state and final_state must be 16-byte
+ * aligned; beta 2-byte; cu_seqlens, A_log, dt_bias 4-byte. When T == 0 the
+ * token tensors (q, k, v, g, beta, o) hold nothing and may be NULL.
+ * Returns KDA_OK when the work was enqueued. Concurrent calls on different
+ * streams are safe when each has its own workspace and outputs.
+ */
+KDA_API kda_status_t kda_fwd(const void *q, const void *k, const void *v, const void *g,
+                     const void *beta, const float *A_log, const float *dt_bias,
+                     float lower_bound, float scale, const float *initial_state,
+                     float *final_state, const int32_t *cu_seqlens, int B, int T,
+                     int H, int K, int V, int num_seqs, void *o, void *workspace,
+                     size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * Stage timing hooks for kda_fwd_with_events(): CUDA events (cudaEvent_t,
+ * created by the caller) recorded on `stream` at the stage boundaries. Any
+ * member may be NULL. prep_start precedes the varlen schedule (if any) and
+ * the prep kernel; prep_done separates the prep kernel from the recurrence
+ * kernel; recur_done follows the recurrence kernel.
+ */
+typedef struct {
+  void *prep_start;
+  void *prep_done;
+  void *recur_done;
+} kda_stage_events_t;
+
+/*
+ * kda_fwd() with stage events recorded for profiling (same arguments, same
+ * results; `events` may be NULL, which makes it identical to kda_fwd()).
+ * Defined by the same operation as kda_fwd(); the events only timestamp the
+ * two kernels the chunked forward is split into (FlashKDA page, section
+ * "커널 퓨전(Kernel Fusion) 전략의 분리").
+ */
+KDA_API kda_status_t kda_fwd_with_events(const void *q, const void *k, const void *v, const void *g,
+                                         const void *beta, const float *A_log, const float *dt_bias,
+                                         float lower_bound, float scale, const float *initial_state,
+                                         float *final_state, const int32_t *cu_seqlens, int B, int T,
+                                         int H, int K, int V, int num_seqs, void *o, void *workspace,
+                                         size_t workspace_bytes, kda_stream_t stream,
+                                         const kda_stage_events_t *events);
+
+/*
+ * Diagnostic entry point: runs only the varlen schedule and the token-parallel
+ * prep kernel of kda_fwd() and copies, for every chunk c (in sequence order,
+ * chunk c of sequence s at index chunk_offset[s] + c, where chunk_offset is the
+ * exclusive prefix sum of ceil(len_s / 64)) and head h, the fp16 matrix
+ *   M[c,h] = [ -Tb ; P Tb ]  (128 x 64, row-major),  Tb = (I + A)^{-1} diag(beta)
+ * into `chunk_mats` (device, fp16 [max_chunks][H][128][64], max_chunks =
+ * kda_max_chunks(B, T, num_seqs)). A, P are the decay-weighted strictly lower
+ * key-key and lower query-key chunk matrices. Rows and columns past the end
+ * of a partial chunk are zero (their beta is taken as 0). Same arguments and
+ * errors as kda_fwd() otherwise.
+ */
+KDA_API kda_status_t kda_debug_chunk_matrices(const void *q, const void *k, const void *g,
+                                      const void *beta, const float *A_log,
+                                      const float *dt_bias, float lower_bound,
+                                      const int32_t *cu_seqlens, int B, int T, int H,
+                                      int K, int num_seqs, void *chunk_mats,
+                                      void *workspace, size_t workspace_bytes,
+                                      kda_stream_t stream);
+
+/* Upper bound on the number of 64-token chunks over all sequences. */
+KDA_API int64_t kda_max_chunks(int B, int T, int num_seqs);
+
+/* Human-readable text of a status code (static storage, never NULL). */
+KDA_API const char *kda_status_string(kda_status_t status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device. Returns KDA_OK if no data error was recorded since the last
+ * read, KDA_ERR_DEVICE_STATUS if one was (its KDA_DEVICE_* code is stored in
+ * *device_code when that pointer is not NULL), or KDA_ERR_CUDA.
+ */
+KDA_API kda_status_t kda_get_device_status(kda_stream_t stream, int *device_code);
+
+/* Library version as major*10000 + minor*100 + patch. */
+KDA_API int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_KDA_H_ */

@@ -1,0 +1,101 @@
+"""The C ABI library: it loads, exports every symbol include/kda.h declares, and
+rejects invalid calls on the host before any CUDA work (no GPU needed)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from chunked_gated_delta_02_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build()
+    from chunked_gated_delta_02_gb300._lib import lib as load
+    return load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
+    return sorted({n for n in names if n.startswith("kda_")})
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for must in ("kda_fwd", "kda_fwd_workspace_size", "kda_status_string", "kda_get_device_status",
+                 "kda_debug_chunk_matrices", "kda_max_chunks", "kda_version"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/kda.h but not exported"
+
+
+def test_bindings_cover_every_symbol():
+    from chunked_gated_delta_02_gb300._lib import SIGNATURES
+    assert sorted(SIGNATURES) == declared_functions()
+
+
+def test_version_and_strings(lib):
+    assert lib.kda_version() >= 100
+    for code in range(6):
+        assert lib.kda_status_string(code)
+    assert lib.kda_status_string(99) == b"unknown status"
+
+
+def test_workspace_size(lib):
+    # fixed length: B*ceil(T/64) + N chunks, 16 KiB per (chunk, head), plus a small header
+    ws = lib.kda_fwd_workspace_size(2, 2048, 32, 128, 128, 2)
+    assert ws >= (2 * 32 + 2) * 32 * 16384
+    assert ws % 256 == 0
+    assert lib.kda_fwd_workspace_size(0, 10, 1, 64, 64, 0) == 0       # B < 1
+    assert lib.kda_fwd_workspace_size(1, -1, 1, 64, 64, 1) == 0       # T < 0
+    assert lib.kda_max_chunks(2, 130, 2) == 2 * 3 + 2
+    assert lib.kda_max_chunks(1, 0, 3) == 3
+
+
+FAKE = 0x10000   # a 256-byte aligned address that is never dereferenced
+
+
+def _call(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, A_log=FAKE, dt_bias=None, lb=-5.0, scale=0.125,
+             init=None, final=None, cu=None, B=1, T=64, H=1, K=64, V=64, N=1, o=FAKE, ws=FAKE,
+             ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.kda_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["A_log"], a["dt_bias"], a["lb"],
+                       a["scale"], a["init"], a["final"], a["cu"], a["B"], a["T"], a["H"], a["K"], a["V"],
+                       a["N"], a["o"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(g=None), 1), (dict(beta=None), 1),
+    (dict(A_log=None), 1), (dict(o=None), 1),
+    (dict(K=96), 2), (dict(V=32), 2), (dict(K=256), 2),
+    (dict(lb=-5.5), 1), (dict(lb=0.5), 1), (dict(lb=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(B=0), 1), (dict(T=-1), 1), (dict(H=0), 1), (dict(N=2), 1),
+    (dict(cu=FAKE, B=2, N=2), 1),
+    (dict(q=FAKE + 8), 1), (dict(o=FAKE + 4), 1), (dict(beta=FAKE + 1), 1), (dict(init=FAKE + 4), 1),
+    (dict(final=FAKE + 8), 1), (dict(cu=FAKE + 2, N=1), 1),
+    (dict(ws_bytes=100), 3), (dict(ws=FAKE + 16), 3),
+])
+def test_host_validation_rejects_without_launch(lib, kw, code):
+    assert _call(lib, **kw) == code
+
+
+def test_null_token_tensors_allowed_only_when_empty(lib):
+    assert _call(lib, q=None, T=5) == 1
+    assert _call(lib, o=None, T=5) == 1
+
+
+def test_zero_sequences_is_a_no_op(lib):
+    # N = 0 packed sequences: nothing to do, no CUDA call is made
+    assert _call(lib, cu=FAKE, N=0, T=0) == 0
