@@ -28,6 +28,7 @@ SIGNATURES = {
     "kda_fwd": (I, [P, P, P, P, P, P, P, F, F, P, P, P, I, I, I, I, I, I, P, P, ctypes.c_size_t, P]),
     "kda_fwd_with_events": (I, [P, P, P, P, P, P, P, F, F, P, P, P, I, I, I, I, I, I, P, P, ctypes.c_size_t, P,
                                  P]),
+    "kda_fwd_noalloc": (I, [P, P, P, P, P, P, P, F, F, P, P, P, I, I, I, I, I, I, P, P]),
     "kda_debug_chunk_matrices": (I, [P, P, P, P, P, P, F, P, I, I, I, I, I, P, P, ctypes.c_size_t, P]),
     "kda_max_chunks": (ctypes.c_int64, [I, I, I]),
     "kda_status_string": (ctypes.c_char_p, [I]),

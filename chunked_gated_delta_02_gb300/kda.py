@@ -15,7 +15,11 @@ import torch
 
 from ._lib import check, lib
 
-__all__ = ["fwd", "workspace_size", "debug_chunk_matrices", "device_status", "max_chunks"]
+__all__ = ["fwd", "fwd_noalloc", "workspace_size", "debug_chunk_matrices", "device_status", "max_chunks",
+           "NOALLOC_MAX_SCRATCH"]
+
+# Size of the library's fixed scratch array used by fwd_noalloc (KDA_NOALLOC_MAX_SCRATCH).
+NOALLOC_MAX_SCRATCH = 16 * 1024 * 1024
 
 
 class _StageEvents(ctypes.Structure):
@@ -115,6 +119,34 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
                                        _stream_ptr(), ev)
     check("kda_fwd", rc)
     return o, fs
+
+
+def fwd_noalloc(q, k, v, g, beta, A_log, dt_bias=None, lower_bound=-5.0, scale=None, initial_state=None,
+                final_state=None, cu_seqlens=None, out=None):
+    """KDA forward through kda_fwd_noalloc: the library allocates nothing.
+
+    For callers that cannot allocate device memory (a runtime that owns the
+    whole pool, or a path where cudaMalloc is not allowed): the scratch is a
+    fixed array inside libkda.so, so the problem must satisfy
+    workspace_size(...) <= NOALLOC_MAX_SCRATCH. The caller passes the output
+    buffers (`out`, bf16 [B,T,H,V]; `final_state`, fp32 [N,H,V,K] or None).
+    Calls that overlap on the GPU share the array and race: keep them ordered.
+    Returns (out, final_state).
+    """
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (A_log, "A_log"), (out, "out")):
+        if t is None or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if scale is None:
+        scale = K ** -0.5
+    with torch.cuda.device(q.device):
+        rc = lib().kda_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+                                   float(lower_bound), float(scale), _ptr(initial_state), _ptr(final_state),
+                                   _ptr(cu_seqlens), B, T, H, K, V, N, _ptr(out), _stream_ptr())
+    check("kda_fwd_noalloc", rc)
+    return out, final_state
 
 
 def debug_chunk_matrices(q, k, g, beta, A_log, dt_bias=None, lower_bound=-5.0, cu_seqlens=None):

@@ -169,6 +169,44 @@ KDA_API kda_status_t kda_debug_chunk_matrices(const void *q, const void *k, cons
                                       void *workspace, size_t workspace_bytes,
                                       kda_stream_t stream);
 
+/*
+ * kda_fwd() for callers that cannot allocate device memory. (This entry point
+ * has no counterpart on the pages; it is a deployment convenience.)
+ *
+ * Who needs it: hosts that own all device memory themselves, such as a
+ * serving runtime that reserves the whole GPU pool at start-up and gives a
+ * kernel plug-in only its inputs and outputs, or a latency-critical path that
+ * must not call cudaMalloc / cudaMallocAsync (they can synchronise the device
+ * or grow a memory pool). Here the scratch that kda_fwd() would take from the
+ * caller lives in a fixed array inside the library image, so the call
+ * allocates nothing: it calls no cudaMalloc, cudaFree or allocating routine.
+ *
+ * Arguments, layouts and results are those of kda_fwd() without the
+ * workspace pair; the caller still passes every input and output buffer.
+ *
+ * Limit: the problem must fit in KDA_NOALLOC_MAX_SCRATCH bytes of scratch,
+ * i.e. kda_fwd_workspace_size(B, T, H, K, V, num_seqs) <= KDA_NOALLOC_MAX_SCRATCH
+ * (for example 16 MiB holds about 1000 (chunk, head) pairs: B=1, T=8192, H=7).
+ * Larger problems are rejected with KDA_ERR_WORKSPACE before anything runs.
+ * Every GPU that loads the library holds this array until the process exits.
+ *
+ * Set-up: the first call on each device looks up the device address of the
+ * array (cudaGetSymbolAddress with that device current). Make that first call
+ * before any stream capture on the device.
+ *
+ * Sharing: all calls on a device share the one array, and it keeps the last
+ * call's contents (no call depends on it starting at zero). Calls whose work
+ * overlaps on the GPU (for example on two streams at once) race on the array
+ * and give wrong results: order them on one stream or synchronise between
+ * them.
+ */
+#define KDA_NOALLOC_MAX_SCRATCH (16u * 1024u * 1024u)
+KDA_API kda_status_t kda_fwd_noalloc(const void *q, const void *k, const void *v, const void *g,
+                                     const void *beta, const float *A_log, const float *dt_bias,
+                                     float lower_bound, float scale, const float *initial_state,
+                                     float *final_state, const int32_t *cu_seqlens, int B, int T,
+                                     int H, int K, int V, int num_seqs, void *o, kda_stream_t stream);
+
 /* Upper bound on the number of 64-token chunks over all sequences. */
 KDA_API int64_t kda_max_chunks(int B, int T, int num_seqs);
 
