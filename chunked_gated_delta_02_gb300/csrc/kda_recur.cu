@@ -1,47 +1,74 @@
-// K2: head-parallel chunk recurrence of the KDA chunked forward.
+// K2: head-parallel chunk recurrence of the KDA chunked forward, on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
-// One CTA per (sequence, head, 32-wide slice of V). The CTA walks the chunks
-// of its sequence in order and carries the K x 32 slice of the state S on
-// chip (the FlashKDA "K2" stage, FlashKDA page, section "커널 퓨전(Kernel
-// Fusion) 전략의 분리"; the cuLA "chunk gated delta h" + "chunk fwd o"
-// stages, cuLA launch blog, section "Status & Roadmap"). Per chunk, with
-// M = [-Tb ; P Tb] from the prep kernel and G the in-chunk cumulative base-2
-// log decay measured from the chunk start:
+// One CTA per (sequence, head, 64-wide slice of V). The CTA walks the chunks
+// of its sequence in order and carries its K x 64 slice of the state S (the
+// FlashKDA "K2" stage, FlashKDA page, section "커널 퓨전(Kernel Fusion) 전략의
+// 분리"; the cuLA "chunk gated delta h" + "chunk fwd o" stages, cuLA launch
+// blog, section "Status & Roadmap"). Per chunk, with M = [-Tb ; P Tb] from
+// the prep kernel and G the in-chunk cumulative decay from the chunk start:
 //
-//   [-w ; P w] = M (khat 2^G)          q~ = qhat 2^G,   Q' = q~ - P w
-//   [-u ; P u] = M v                    k~ = khat 2^{G_last - G},  gamma = 2^{G_last}
-//   R = [-u ; P u] + [w ; Q'] S        ->  U = -R[0:64],  o = scale R[64:128]
-//   S <- Diag(gamma) S + k~^T U
+//   D1 = M (khat 2^G)            = [-w ; P w]        (128 x K,  UMMA 128xKx64)
+//   D2 = M v                     = [-u ; P u]        (128 x 64, UMMA 128x64x64)
+//   WQ = [w ; q~ - P w],  q~ = qhat 2^G              (threads, fp16)
+//   D2 += WQ S                   = [-U ; O]          (UMMA 128x64xK)
+//   U -> fp16, o = scale O -> bf16                   (threads)
+//   D3 = k~^T U,  k~ = khat 2^{G_last - G}           (UMMA 128x64x64)
+//   S  = 2^{G_last} S + D3                           (threads, fp32 master in registers)
 //
-// which is the WY/UT form of the delta rule inside a chunk: U are the
-// residuals v - prediction, o mixes the inter-chunk term q~ S with the
-// intra-chunk term P U. All factors 2^G, 2^{G_last-G} are <= 1.
-// This version computes in fp32 on the CUDA cores.
+// U holds the delta-rule residuals v - prediction of the chunk, O the
+// inter-chunk term q~ S plus the intra-chunk term P U. The decays 2^G and
+// 2^{G_last-G} are prefix/suffix products of the per-token alpha, all <= 1.
+// Operands are fp16 in shared memory (128-byte swizzled canonical layouts),
+// accumulators fp32 in tensor memory; the state master copy stays fp32 in
+// registers (thread k owns row k of S) and an fp16 copy feeds the next chunk.
 #include "kda_common.cuh"
+#include "umma.cuh"
 
 namespace kda {
 
-constexpr int kRecThreads = 256;
-constexpr int kBV = 32;
+constexpr int kRecThreads = 128;
+constexpr int kBV = 64;
+constexpr uint32_t kTmemCols = 256;
+constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clocks per wait
 
 template <int K>
-struct RecSmem {
-  static constexpr int KP = K + 1;
-  float bufA[kChunk][KP];   // khat 2^G, then v tile / U
-  float bufB[kChunk][KP];   // q~, then Q'
-  float bufC[kChunk][KP];   // G, then k~
-  float bufD[kChunk][KP];   // khat, then w
-  float M[2 * kChunk][kChunk + 1];
-  float S[K][kBV + 1];
-  float gam[K];
-  float kn[kChunk], qn[kChunk];
+struct RecLayout {
+  // byte offsets from the 1024-aligned dynamic shared memory base
+  static constexpr uint32_t kPanel64 = 64 * 128;                 // 64 rows x 128 B
+  static constexpr uint32_t Mh = 0;                              // 128 x 64  K-major (A of D1, D2)
+  static constexpr uint32_t kG = Mh + 128 * 128;                 // 64 x K    MN-major (B of D1)
+  static constexpr uint32_t vh = kG + (K / 64) * kPanel64;       // 64 x 64   MN-major (B of D2)
+  static constexpr uint32_t WQ = vh + kPanel64;                  // 128 x K   K-major (A of MMA1)
+  static constexpr uint32_t Sh = WQ + (K / 64) * 128 * 128;      // K x 64    MN-major (B of MMA1)
+  static constexpr uint32_t kT = Sh + K * 128;                   // 64 x 128  MN-major (A of MMA2)
+  static constexpr uint32_t Uh = kT + 2 * kPanel64;              // 64 x 64   MN-major (B of MMA2)
+  static constexpr uint32_t qt = Uh + kPanel64;                  // fp32 [64][K]
+  static constexpr uint32_t misc = qt + 64 * K * 4;
+  static constexpr uint32_t bytes = misc + 1024 + 1024;          // + misc + alignment slack
+  static_assert(64 * K * 4 <= (K / 64) * 128 * 128, "alpha scratch must fit in WQ");
 };
 
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
 template <int K>
-__global__ void __launch_bounds__(kRecThreads)
-recur_simt_kernel(const Problem p) {
+__global__ void __launch_bounds__(kRecThreads, 1)
+recur_tc_kernel(const Problem p) {
+  using Lay = RecLayout<K>;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  RecSmem<K> &sm = *reinterpret_cast<RecSmem<K> *>(smem_raw);
+  unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                        ~static_cast<uintptr_t>(1023));
+  float *qt = reinterpret_cast<float *>(sm + Lay::qt);
+  float *alpha_s = reinterpret_cast<float *>(sm + Lay::WQ);   // per-channel pass scratch
+  float *kn = reinterpret_cast<float *>(sm + Lay::misc);
+  float *qn = kn + 64;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(qn + 64);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
+  int *s_err = reinterpret_cast<int *>(tmem_slot + 1);
+
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int VT = p.V / kBV;
   const int bid = blockIdx.x;
@@ -51,30 +78,73 @@ recur_simt_kernel(const Problem p) {
   if (p.flag && *p.flag != kDevOk) return;
   const int s = p.cu ? p.order[r] : r;
   const SeqInfo si = seq_info(p, s);
-  // v tile and U reuse bufA (khat 2^G is dead by then): 2 * 64 * 32 floats <= 64 * (K+1)
-  float *vt = &sm.bufA[0][0];
-  float *U = vt + kChunk * kBV;
-  static_assert(2 * kChunk * kBV <= kChunk * (K + 1), "v tile + U must fit in bufA");
+  const uint32_t sbase = umma::smem_u32(sm);
 
-  // state slice: S[k][v] = state[s,h,v0+v,k]
-  for (int x = tid; x < K * kBV; x += kRecThreads) {
-    const int kk = x % K, vv = x / K;
-    sm.S[kk][vv] = p.init ? p.init[(((long long)s * p.H + h) * p.V + v0 + vv) * K + kk] : 0.f;
+  // ---- set-up: zero the k~ operand (rows >= K stay zero when K = 64), TMEM, barrier
+  for (int x = tid; x < (int)(2 * Lay::kPanel64 / 16); x += kRecThreads)
+    reinterpret_cast<uint4 *>(sm + Lay::kT)[x] = make_uint4(0, 0, 0, 0);
+  if (warp == 0) {
+    umma::tmem_alloc(tmem_slot, kTmemCols);
+    umma::tmem_relinquish();
   }
+  if (tid == 0) {
+    umma::mbar_init(bar, 1);
+    umma::mbar_fence_init();
+    *s_err = 0;
+  }
+
+  // state master: thread k owns S[k][0:64] (fp32), also written as the fp16 operand
+  float S[kBV];
+  if (tid < K) {
+#pragma unroll
+    for (int v = 0; v < kBV; ++v)
+      S[v] = p.init ? p.init[(((long long)s * p.H + h) * p.V + v0 + v) * K + tid] : 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4 w;
+      w.x = pack_half2(S[8 * c + 0], S[8 * c + 1]);
+      w.y = pack_half2(S[8 * c + 2], S[8 * c + 3]);
+      w.z = pack_half2(S[8 * c + 4], S[8 * c + 5]);
+      w.w = pack_half2(S[8 * c + 6], S[8 * c + 7]);
+      *reinterpret_cast<uint4 *>(sm + Lay::Sh + umma::sw128_chunk(tid, c)) = w;
+    }
+  }
+  umma::fence_proxy_async_smem();
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tD1 = tmem, tD2 = tmem + 128, tD3 = tmem + 192;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+
   const float ea = expf(p.A_log[h]);
   const float lbl2 = p.lb * kLog2e;
+  const float dt = (tid < K && p.dt_bias) ? p.dt_bias[h * K + tid] : 0.f;
   const int nch = (si.len + kChunk - 1) / kChunk;
-  __syncthreads();
+  uint32_t phase = 0;
+  float gam = 1.f;
 
-  for (int n = 0; n < nch; ++n) {
+  // Bounded wait on the MMA barrier; every thread learns whether anyone timed out.
+  auto wait_mma = [&]() -> bool {
+    if (!umma::mbar_wait_bounded(bar, phase, kWaitLimit)) atomicExch(s_err, 1);
+    phase ^= 1u;
+    __syncthreads();
+    umma::fence_after_sync();
+    return *s_err == 0;
+  };
+
+  bool ok = true;
+  for (int n = 0; n < nch && ok; ++n) {
     const int t0 = si.t0 + n * kChunk;
     const int L = min(kChunk, si.len - n * kChunk);
     const long long cidx = (long long)si.chunk0 + n;
-    // -- norms
+
+    // ---- A1: row norms; hand-off matrix and v tile into their operand layouts
     for (int i = warp; i < kChunk; i += kRecThreads / 32) {
       float ssk = 0.f, ssq = 0.f;
       if (i < L) {
         const long long row = tok_row(p, si.b, t0 + i, h);
+#pragma unroll
         for (int kk = lane; kk < K; kk += 32) {
           const float a = __bfloat162float(p.k[row * K + kk]), b = __bfloat162float(p.q[row * K + kk]);
           ssk += a * a;
@@ -84,104 +154,217 @@ recur_simt_kernel(const Problem p) {
       ssk = warp_sum(ssk);
       ssq = warp_sum(ssq);
       if (lane == 0) {
-        sm.kn[i] = (i < L) ? rsqrtf(ssk + kNormEps) : 0.f;
-        sm.qn[i] = (i < L) ? rsqrtf(ssq + kNormEps) : 0.f;
+        kn[i] = (i < L) ? rsqrtf(ssk + kNormEps) : 0.f;
+        qn[i] = (i < L) ? rsqrtf(ssq + kNormEps) : 0.f;
       }
     }
-    __syncthreads();
-    // -- per-channel cumulative decay and decayed operands
-    if (tid < K) {
-      const int kk = tid;
-      const float dt = p.dt_bias ? p.dt_bias[h * K + kk] : 0.f;
-      float G = 0.f;
-      for (int i = 0; i < kChunk; ++i) {
-        float kv = 0.f, qv = 0.f;
-        if (i < L) {
-          const long long row = tok_row(p, si.b, t0 + i, h);
-          G += log2_decay(__bfloat162float(p.g[row * K + kk]), dt, ea, lbl2);
-          kv = __bfloat162float(p.k[row * K + kk]) * sm.kn[i];
-          qv = __bfloat162float(p.q[row * K + kk]) * sm.qn[i];
-        }
-        const float X = ex2_approx(G);
-        sm.bufA[i][kk] = kv * X;
-        sm.bufB[i][kk] = qv * X;
-        sm.bufC[i][kk] = G;
-        sm.bufD[i][kk] = kv;
-      }
-      sm.gam[kk] = ex2_approx(G);
-      for (int i = 0; i < kChunk; ++i) sm.bufC[i][kk] = sm.bufD[i][kk] * ex2_approx(G - sm.bufC[i][kk]);
-    }
-    // -- hand-off matrix of this chunk
     {
       const uint4 *src = reinterpret_cast<const uint4 *>(p.mats + (cidx * p.H + h) * (2 * kChunk * kChunk));
-      for (int x = tid; x < 2 * kChunk * kChunk / 8; x += kRecThreads) {
-        const uint4 u = src[x];
-        const __half *hv = reinterpret_cast<const __half *>(&u);
-        const int rr = (x * 8) / kChunk, cc = (x * 8) % kChunk;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) sm.M[rr][cc + e] = __half2float(hv[e]);
+      for (int j = 0; j < 8; ++j) {
+        const int x = tid + kRecThreads * j;   // 16-byte chunk: row x / 8, chunk x % 8
+        *reinterpret_cast<uint4 *>(sm + Lay::Mh + umma::sw128_chunk(x >> 3, x & 7)) = src[x];
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int x = tid + kRecThreads * j;   // v tile: row x / 8, 8 values from column 8 * (x % 8)
+        const int i = x >> 3, c = x & 7;
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (i < L) {
+          const uint4 raw = *reinterpret_cast<const uint4 *>(
+              p.v + tok_row(p, si.b, t0 + i, h) * p.V + v0 + 8 * c);
+          const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+          float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]);
+          float2 f2 = __bfloat1622float2(b2[2]), f3 = __bfloat1622float2(b2[3]);
+          w = make_uint4(pack_half2(f0.x, f0.y), pack_half2(f1.x, f1.y), pack_half2(f2.x, f2.y),
+                         pack_half2(f3.x, f3.y));
+        }
+        *reinterpret_cast<uint4 *>(sm + Lay::vh + umma::sw128_chunk(i, c)) = w;
       }
     }
     __syncthreads();
-    // -- [-w ; P w] = M (khat 2^G)
-    for (int x = tid; x < 2 * kChunk * K; x += kRecThreads) {
-      const int kk = x % K, rr = x / K;
-      float acc = 0.f;
-#pragma unroll 8
-      for (int j = 0; j < kChunk; ++j) acc += sm.M[rr][j] * sm.bufA[j][kk];
-      if (rr < kChunk) sm.bufD[rr][kk] = -acc;
-      else sm.bufB[rr - kChunk][kk] -= acc;
+
+    // ---- A2: per-channel gate, prefix/suffix decay products, decayed operands (thread = channel)
+    if (tid < K) {
+      const int kk = tid;
+      const uint32_t col_off = (uint32_t)(kk >> 6) * Lay::kPanel64;
+      float Gam = 1.f;
+      for (int i = 0; i < kChunk; ++i) {
+        float kv = 0.f, qv = 0.f, al = 1.f;
+        if (i < L) {
+          const long long row = tok_row(p, si.b, t0 + i, h);
+          al = ex2_approx(log2_decay(__bfloat162float(p.g[row * K + kk]), dt, ea, lbl2));
+          kv = __bfloat162float(p.k[row * K + kk]) * kn[i];
+          qv = __bfloat162float(p.q[row * K + kk]) * qn[i];
+          Gam *= al;
+        }
+        alpha_s[i * K + kk] = al;
+        *reinterpret_cast<__half *>(sm + Lay::kG + col_off + umma::sw128_offset(i, kk & 63)) =
+            __float2half_rn(kv * Gam);
+        qt[i * K + kk] = qv * Gam;
+      }
+      gam = Gam;
+      float suf = 1.f;
+      for (int i = kChunk - 1; i >= 0; --i) {
+        float kv = 0.f;
+        if (i < L) kv = __bfloat162float(p.k[tok_row(p, si.b, t0 + i, h) * K + kk]) * kn[i];
+        *reinterpret_cast<__half *>(sm + Lay::kT + col_off + umma::sw128_offset(i, kk & 63)) =
+            __float2half_rn(kv * suf);
+        suf *= alpha_s[i * K + kk];
+      }
     }
+    umma::fence_proxy_async_smem();
+    umma::fence_before_sync();
     __syncthreads();
-    // -- v tile
-    for (int x = tid; x < kChunk * kBV; x += kRecThreads) {
-      const int vv = x % kBV, i = x / kBV;
-      vt[i * kBV + vv] = (i < L) ? __bfloat162float(p.v[tok_row(p, si.b, t0 + i, h) * p.V + v0 + vv]) : 0.f;
+
+    // ---- B: D1 = M (khat 2^G), D2 = M v
+    if (tid == 0) {
+      umma::fence_after_sync();
+      const uint32_t id1 = umma::idesc_f16(128, K, 0, 1), id2 = umma::idesc_f16(128, kBV, 0, 1);
+#pragma unroll
+      for (int ks = 0; ks < kChunk / 16; ++ks) {
+        const uint64_t a = umma::sdesc_sw128(sbase + Lay::Mh + ks * 32, 16, 1024);
+        umma::mma_f16_ss(tD1, a, umma::sdesc_sw128(sbase + Lay::kG + ks * 2048, Lay::kPanel64, 1024), id1, ks > 0);
+        umma::mma_f16_ss(tD2, a, umma::sdesc_sw128(sbase + Lay::vh + ks * 2048, Lay::kPanel64, 1024), id2, ks > 0);
+      }
+      umma::commit(bar);
     }
-    __syncthreads();
-    // -- R = M v + [w ; Q'] S ; o = scale R[64:], U = -R[:64]
-    for (int x = tid; x < 2 * kChunk * kBV; x += kRecThreads) {
-      const int vv = x % kBV, rr = x / kBV;
-      float acc = 0.f;
-#pragma unroll 8
-      for (int j = 0; j < kChunk; ++j) acc += sm.M[rr][j] * vt[j * kBV + vv];
-      const float *X = (rr < kChunk) ? &sm.bufD[rr][0] : &sm.bufB[rr - kChunk][0];
-#pragma unroll 8
-      for (int kk = 0; kk < K; ++kk) acc += X[kk] * sm.S[kk][vv];
-      if (rr < kChunk) {
-        U[rr * kBV + vv] = -acc;
+    if (!(ok = wait_mma())) break;
+
+    // ---- C: WQ rows: w = -D1 (rows < 64), Q' = q~ - D1 (rows >= 64)
+#pragma unroll 1
+    for (int c0 = 0; c0 < K; c0 += 16) {
+      float x[16];
+      umma::tmem_ld16(tD1 + lane_base + c0, x);
+      umma::tmem_ld_wait();
+      if (tid < kChunk) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = -x[j];
       } else {
-        const int i = rr - kChunk;
-        if (i < L) p.o[tok_row(p, si.b, t0 + i, h) * p.V + v0 + vv] = __float2bfloat16_rn(p.scale * acc);
+        const float *qr = qt + (tid - kChunk) * K + c0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = qr[j] - x[j];
+      }
+      const uint32_t pan = Lay::WQ + (uint32_t)(c0 >> 6) * (128 * 128);
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        uint4 w;
+        w.x = pack_half2(x[8 * hc + 0], x[8 * hc + 1]);
+        w.y = pack_half2(x[8 * hc + 2], x[8 * hc + 3]);
+        w.z = pack_half2(x[8 * hc + 4], x[8 * hc + 5]);
+        w.w = pack_half2(x[8 * hc + 6], x[8 * hc + 7]);
+        *reinterpret_cast<uint4 *>(sm + pan + umma::sw128_chunk(tid, ((c0 & 63) >> 3) + hc)) = w;
       }
     }
+    umma::fence_proxy_async_smem();
+    umma::fence_before_sync();
     __syncthreads();
-    // -- S <- Diag(gamma) S + k~^T U
-    for (int x = tid; x < K * kBV; x += kRecThreads) {
-      const int vv = x % kBV, kk = x / kBV;
-      float acc = 0.f;
-#pragma unroll 8
-      for (int i = 0; i < kChunk; ++i) acc += sm.bufC[i][kk] * U[i * kBV + vv];
-      sm.S[kk][vv] = sm.gam[kk] * sm.S[kk][vv] + acc;
+
+    // ---- D: D2 += WQ S  ->  [-U ; O]
+    if (tid == 0) {
+      umma::fence_after_sync();
+      const uint32_t id = umma::idesc_f16(128, kBV, 0, 1);
+#pragma unroll
+      for (int ks = 0; ks < K / 16; ++ks) {
+        const uint64_t a = umma::sdesc_sw128(sbase + Lay::WQ + (ks >> 2) * (128 * 128) + (ks & 3) * 32, 16, 1024);
+        const uint64_t b = umma::sdesc_sw128(sbase + Lay::Sh + ks * 2048, K * 128, 1024);
+        umma::mma_f16_ss(tD2, a, b, id, 1);
+      }
+      umma::commit(bar);
     }
+    if (!(ok = wait_mma())) break;
+
+    // ---- E: U (rows < 64) -> fp16 operand; o = scale * O (rows >= 64) -> bf16 global
+#pragma unroll 1
+    for (int c0 = 0; c0 < kBV; c0 += 16) {
+      float x[16];
+      umma::tmem_ld16(tD2 + lane_base + c0, x);
+      umma::tmem_ld_wait();
+      if (tid < kChunk) {
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          uint4 w;
+          w.x = pack_half2(-x[8 * hc + 0], -x[8 * hc + 1]);
+          w.y = pack_half2(-x[8 * hc + 2], -x[8 * hc + 3]);
+          w.z = pack_half2(-x[8 * hc + 4], -x[8 * hc + 5]);
+          w.w = pack_half2(-x[8 * hc + 6], -x[8 * hc + 7]);
+          *reinterpret_cast<uint4 *>(sm + Lay::Uh + umma::sw128_chunk(tid, (c0 >> 3) + hc)) = w;
+        }
+      } else if (tid - kChunk < L) {
+        __nv_bfloat16 ob[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ob[j] = __float2bfloat16_rn(p.scale * x[j]);
+        uint4 *dst = reinterpret_cast<uint4 *>(p.o + tok_row(p, si.b, t0 + tid - kChunk, h) * p.V + v0 + c0);
+        dst[0] = *reinterpret_cast<const uint4 *>(&ob[0]);
+        dst[1] = *reinterpret_cast<const uint4 *>(&ob[8]);
+      }
+    }
+    umma::fence_proxy_async_smem();
+    umma::fence_before_sync();
+    __syncthreads();
+
+    // ---- F: D3 = k~^T U
+    if (tid == 0) {
+      umma::fence_after_sync();
+      const uint32_t id = umma::idesc_f16(128, kBV, 1, 1);
+#pragma unroll
+      for (int ks = 0; ks < kChunk / 16; ++ks) {
+        const uint64_t a = umma::sdesc_sw128(sbase + Lay::kT + ks * 2048, Lay::kPanel64, 1024);
+        const uint64_t b = umma::sdesc_sw128(sbase + Lay::Uh + ks * 2048, Lay::kPanel64, 1024);
+        umma::mma_f16_ss(tD3, a, b, id, ks > 0);
+      }
+      umma::commit(bar);
+    }
+    if (!(ok = wait_mma())) break;
+
+    // ---- G: S = gamma S + D3 (thread = channel), fp16 copy for the next chunk
+    if (tid < K) {
+#pragma unroll
+      for (int c0 = 0; c0 < kBV; c0 += 16) {
+        float x[16];
+        umma::tmem_ld16(tD3 + lane_base + c0, x);
+        umma::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) S[c0 + j] = fmaf(gam, S[c0 + j], x[j]);
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          uint4 w;
+          const float *sv = &S[c0 + 8 * hc];
+          w.x = pack_half2(sv[0], sv[1]);
+          w.y = pack_half2(sv[2], sv[3]);
+          w.z = pack_half2(sv[4], sv[5]);
+          w.w = pack_half2(sv[6], sv[7]);
+          *reinterpret_cast<uint4 *>(sm + Lay::Sh + umma::sw128_chunk(tid, (c0 >> 3) + hc)) = w;
+        }
+      }
+    }
+    umma::fence_proxy_async_smem();
+    umma::fence_before_sync();
     __syncthreads();
   }
-  if (p.final_state) {
-    for (int x = tid; x < K * kBV; x += kRecThreads) {
-      const int kk = x % K, vv = x / K;
-      p.final_state[(((long long)s * p.H + h) * p.V + v0 + vv) * K + kk] = sm.S[kk][vv];
-    }
+
+  if (!ok) {
+    if (tid == 0) atomicExch(p.dev_status, kDevWaitTimeout);
+    // one more bounded wait (on the phase that timed out) so that no MMA of
+    // this CTA is still writing TMEM when it is released
+    umma::mbar_wait_bounded(bar, phase ^ 1u, kWaitLimit);
+  } else if (p.final_state && tid < K) {
+#pragma unroll
+    for (int v = 0; v < kBV; ++v) p.final_state[(((long long)s * p.H + h) * p.V + v0 + v) * K + tid] = S[v];
   }
+  umma::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int K>
 static cudaError_t launch_recur_t(const Problem &p, cudaStream_t stream) {
-  const size_t smem = sizeof(RecSmem<K>);
-  cudaError_t e = cudaFuncSetAttribute(recur_simt_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t smem = RecLayout<K>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(recur_tc_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)p.N * p.H * (p.V / kBV);
-  recur_simt_kernel<K><<<(unsigned)grid, kRecThreads, smem, stream>>>(p);
+  recur_tc_kernel<K><<<(unsigned)grid, kRecThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
