@@ -104,6 +104,30 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// 16-byte global -> shared asynchronous copy (L2 only); src_valid == false zero-fills.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool src_valid) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem),
+               "r"(src_valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+// Stage rows [0, 64) of a chunk of a [B,T,H,D] bf16 tensor into shared memory
+// as bf16 [64][D] (rows >= L zero-filled). D * 2 bytes must be a multiple of 16.
+template <int D, int NT>
+__device__ __forceinline__ void stage_rows_async(__nv_bfloat16 *dst, const __nv_bfloat16 *src, const Problem &p,
+                                                 int b, int t0, int h, int L, int col0, int ld, int tid) {
+  constexpr int kChunks = D * 2 / 16;   // 16-byte chunks per row
+  for (int x = tid; x < kChunk * kChunks; x += NT) {
+    const int i = x / kChunks, c = x % kChunks;
+    const bool ok = i < L;
+    const __nv_bfloat16 *g = ok ? src + tok_row(p, b, t0 + i, h) * ld + col0 + c * 8 : src;
+    cp_async16(dst + i * D + c * 8, g, ok);
+  }
+}
+
 // Global chunk index -> sequence (binary search over the varlen chunk offsets).
 __device__ __forceinline__ int chunk_to_seq(const Problem &p, long long c) {
   if (!p.cu) return (int)(c / p.nc_fixed);

@@ -27,23 +27,42 @@
 // This is the "intra-chunk rescaling" that large chunks need (FlashKDA page,
 // section "Flash Linear Attention과 비교"); the block products run on the
 // tensor cores in tf32 (mma.sync m16n8k8, operands rounded to nearest).
+//
+// The unit lower triangular inverse T = (I + A)^{-1} is blocked: the four
+// 16 x 16 diagonal blocks by right-looking forward substitution (one thread
+// per column, the column held in registers), then the off-diagonal blocks
+// level by level, T_IJ = -T_II sum_{J<=M<I} A_IM T_MJ, in fp32.
 #include "kda_common.cuh"
 
 namespace kda {
 
-constexpr int kPrepThreads = 128;
+constexpr int kPrepThreads = 256;
 
 template <int K>
 struct PrepSmem {
-  static constexpr int KP = K + 4;   // padded row stride (floats): conflict-free fragment loads
-  float kX[kChunk][KP];              // khat * 2^{Gb}
-  float qX[kChunk][KP];              // qhat * 2^{Gb}
-  float kY[kChunk][KP];              // khat * 2^{-Gb}
-  float eB[4][K];                    // 2^{B_J}
-  float c12[K];                      // 2^{B_1 + B_2}
-  float A[kChunk][kChunk + 1];
-  float P[kChunk][kChunk + 1];
-  float Tm[kChunk][kChunk + 1];
+  static constexpr int KF = K + 4;   // fp32 row stride (floats)
+  static constexpr int LD = kChunk + 1;
+  union {
+    struct {                          // passes 0-2: raw staged inputs
+      __nv_bfloat16 q[kChunk * K], k[kChunk * K], g[kChunk * K];
+    } raw;
+    struct {                          // passes 3-5: chunk matrices
+      float A[kChunk][LD], P[kChunk][LD], T[kChunk][LD];
+    } mat;
+  } u1;
+  union {
+    struct {                          // passes 2-3: decay-scaled operands, fp32: in diagonal
+      float kX[kChunk][KF], qX[kChunk][KF];   // blocks the tiny 2^{Gb_i} meets 2^{-Gb_j} up to
+      float kY[kChunk][KF];                   // 2^115, so neither side may flush to zero
+    } op;
+    struct {                          // passes 4-5
+      float Z[3][16][17];
+      __half out[2 * kChunk][kChunk];
+    } post;
+  } u2;
+  float Bs[4][K];                     // whole-block log2 decay B_J
+  float eB[4][K];                     // 2^{B_J}
+  float c12[K];                       // 2^{B_1 + B_2}
   float kn[kChunk], qn[kChunk], beta[kChunk];
 };
 
@@ -58,7 +77,7 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
 __device__ __forceinline__ uint32_t tf32_bits(float x) { return __float_as_uint(to_tf32(x)); }
 
 template <int K>
-__global__ void __launch_bounds__(kPrepThreads)
+__global__ void __launch_bounds__(kPrepThreads, 1)
 prep_kernel(const Problem p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   PrepSmem<K> &sm = *reinterpret_cast<PrepSmem<K> *>(smem_raw);
@@ -74,158 +93,175 @@ prep_kernel(const Problem p) {
   const int t0 = si.t0 + n * kChunk;
   const int len = min(kChunk, si.len - n * kChunk);
 
-  // ---- pass 1: row norms and beta (one warp per row, lanes across channels)
+  // ---- pass 0: stage q, k, g rows (zero-filled past the chunk end); beta sigmoid
+  stage_rows_async<K, kPrepThreads>(sm.u1.raw.q, p.q, p, si.b, t0, h, len, 0, K, tid);
+  stage_rows_async<K, kPrepThreads>(sm.u1.raw.k, p.k, p, si.b, t0, h, len, 0, K, tid);
+  stage_rows_async<K, kPrepThreads>(sm.u1.raw.g, p.g, p, si.b, t0, h, len, 0, K, tid);
+  cp_async_commit();
+  if (tid < kChunk)
+    sm.beta[tid] = (tid < len) ? sigmoid_fast(__bfloat162float(p.beta[tok_row(p, si.b, t0 + tid, h)])) : 0.f;
+  cp_async_wait_all();
+  __syncthreads();
+
+  // ---- pass 1: row norms (one warp per row, lanes across channels)
   for (int i = warp; i < kChunk; i += kPrepThreads / 32) {
-    float ssk = 0.f, ssq = 0.f, bt = 0.f;
-    if (i < len) {
-      const long long row = tok_row(p, si.b, t0 + i, h);
-      const __nv_bfloat16 *kr = p.k + row * K, *qr = p.q + row * K;
+    float ssk = 0.f, ssq = 0.f;
+    const __nv_bfloat162 *kr = reinterpret_cast<const __nv_bfloat162 *>(sm.u1.raw.k + i * K);
+    const __nv_bfloat162 *qr = reinterpret_cast<const __nv_bfloat162 *>(sm.u1.raw.q + i * K);
 #pragma unroll
-      for (int kk = lane; kk < K; kk += 32) {
-        const float a = __bfloat162float(kr[kk]), b = __bfloat162float(qr[kk]);
-        ssk += a * a;
-        ssq += b * b;
-      }
-      bt = sigmoid_fast(__bfloat162float(p.beta[row]));
+    for (int x = lane; x < K / 2; x += 32) {
+      const float2 a = __bfloat1622float2(kr[x]), b = __bfloat1622float2(qr[x]);
+      ssk += a.x * a.x + a.y * a.y;
+      ssq += b.x * b.x + b.y * b.y;
     }
     ssk = warp_sum(ssk);
     ssq = warp_sum(ssq);
     if (lane == 0) {
       sm.kn[i] = (i < len) ? rsqrtf(ssk + kNormEps) : 0.f;
       sm.qn[i] = (i < len) ? rsqrtf(ssq + kNormEps) : 0.f;
-      sm.beta[i] = bt;
     }
-  }
-  // zero A and P (upper blocks stay zero)
-  for (int x = tid; x < kChunk * (kChunk + 1); x += kPrepThreads) {
-    (&sm.A[0][0])[x] = 0.f;
-    (&sm.P[0][0])[x] = 0.f;
   }
   __syncthreads();
 
-  // ---- pass 2: per-channel gate, block-local cumulative decay, scaled operands
-  if (tid < K) {
-    const int kk = tid;
+  // ---- pass 2: per (channel, 16-row block): gate, block-local cumulative decay, scaled operands
+  {
     const float ea = expf(p.A_log[h]);
-    const float dt = p.dt_bias ? p.dt_bias[h * K + kk] : 0.f;
     const float lbl2 = p.lb * kLog2e;
-    float Bsum[4];
-#pragma unroll 1
-    for (int J = 0; J < 4; ++J) {
+    constexpr int kBlocksPerThread = 4 * K / kPrepThreads;   // 2 for K=128, 1 for K=64
+    const int kk = tid % K;
+    const float dt = p.dt_bias ? p.dt_bias[h * K + kk] : 0.f;
+#pragma unroll
+    for (int bj = 0; bj < kBlocksPerThread; ++bj) {
+      const int J = (tid / K) * kBlocksPerThread + bj;
       float Gb = 0.f;
 #pragma unroll 4
       for (int r = 0; r < 16; ++r) {
         const int i = 16 * J + r;
-        float kv = 0.f, qv = 0.f;
-        if (i < len) {
-          const long long row = tok_row(p, si.b, t0 + i, h);
-          Gb += log2_decay(__bfloat162float(p.g[row * K + kk]), dt, ea, lbl2);
-          kv = __bfloat162float(p.k[row * K + kk]) * sm.kn[i];
-          qv = __bfloat162float(p.q[row * K + kk]) * sm.qn[i];
-        }
+        if (i < len) Gb += log2_decay(__bfloat162float(sm.u1.raw.g[i * K + kk]), dt, ea, lbl2);
+        const float kv = __bfloat162float(sm.u1.raw.k[i * K + kk]) * sm.kn[i];
+        const float qv = __bfloat162float(sm.u1.raw.q[i * K + kk]) * sm.qn[i];
         const float X = ex2_approx(Gb), Y = ex2_approx(-Gb);
-        sm.kX[i][kk] = kv * X;
-        sm.qX[i][kk] = qv * X;
-        sm.kY[i][kk] = kv * Y;
+        sm.u2.op.kX[i][kk] = kv * X;
+        sm.u2.op.qX[i][kk] = qv * X;
+        sm.u2.op.kY[i][kk] = kv * Y;
       }
-      Bsum[J] = Gb;
+      sm.Bs[J][kk] = Gb;
       sm.eB[J][kk] = ex2_approx(Gb);
     }
-    sm.c12[kk] = ex2_approx(Bsum[1] + Bsum[2]);
   }
   __syncthreads();
+  if (tid < K) sm.c12[tid] = ex2_approx(sm.Bs[1][tid] + sm.Bs[2][tid]);
+  __syncthreads();   // the raw inputs are dead from here on: A/P/T reuse their space
 
-  // ---- pass 3: A and P block products on the tensor cores (tf32)
-  const int gq = lane >> 2, tq = lane & 3;
-  for (int pr = warp; pr < 10; pr += kPrepThreads / 32) {
-    // pair index -> (I, J), J <= I: (0,0) (1,0) (1,1) (2,0) (2,1) (2,2) (3,0) ...
-    int I = 0;
-    while ((I + 1) * (I + 2) / 2 <= pr) ++I;
-    const int J = pr - I * (I + 1) / 2;
-    float accA[2][4] = {}, accP[2][4] = {};
-#pragma unroll 2
-    for (int k0 = 0; k0 < K; k0 += 8) {
-      const int ka = k0 + tq, kb = k0 + tq + 4;
-      float cia = 1.f, cib = 1.f, sja = 1.f, sjb = 1.f;
-      if (I != J) {
-        sja = sm.eB[J][ka];
-        sjb = sm.eB[J][kb];
-        if (I - J == 2) { cia = sm.eB[J + 1][ka]; cib = sm.eB[J + 1][kb]; }
-        if (I - J == 3) { cia = sm.c12[ka]; cib = sm.c12[kb]; }
+  // ---- pass 3: A and P block products on the tensor cores (tf32); items = (block pair, n-tile)
+  {
+    const int gq = lane >> 2, tq = lane & 3;
+    for (int item = warp; item < 20; item += kPrepThreads / 32) {
+      const int pr = item >> 1, nt = item & 1;
+      int I = 0;
+      while ((I + 1) * (I + 2) / 2 <= pr) ++I;   // pair index -> (I, J), J <= I
+      const int J = pr - I * (I + 1) / 2;
+      float accA[4] = {0.f, 0.f, 0.f, 0.f}, accP[4] = {0.f, 0.f, 0.f, 0.f};
+      const int r0 = 16 * I + gq, r1 = r0 + 8, jr = 16 * J + 8 * nt + gq;
+#pragma unroll 4
+      for (int k0 = 0; k0 < K; k0 += 8) {
+        const int ka = k0 + tq, kb = k0 + tq + 4;
+        float cia = 1.f, cib = 1.f, sja = 1.f, sjb = 1.f;
+        if (I != J) {
+          sja = sm.eB[J][ka];
+          sjb = sm.eB[J][kb];
+          if (I - J == 2) { cia = sm.eB[J + 1][ka]; cib = sm.eB[J + 1][kb]; }
+          if (I - J == 3) { cia = sm.c12[ka]; cib = sm.c12[kb]; }
+        }
+        uint32_t aK[4], aQ[4], b[2];
+        aK[0] = tf32_bits(sm.u2.op.kX[r0][ka] * cia);
+        aK[1] = tf32_bits(sm.u2.op.kX[r1][ka] * cia);
+        aK[2] = tf32_bits(sm.u2.op.kX[r0][kb] * cib);
+        aK[3] = tf32_bits(sm.u2.op.kX[r1][kb] * cib);
+        aQ[0] = tf32_bits(sm.u2.op.qX[r0][ka] * cia);
+        aQ[1] = tf32_bits(sm.u2.op.qX[r1][ka] * cia);
+        aQ[2] = tf32_bits(sm.u2.op.qX[r0][kb] * cib);
+        aQ[3] = tf32_bits(sm.u2.op.qX[r1][kb] * cib);
+        b[0] = tf32_bits(sm.u2.op.kY[jr][ka] * sja);
+        b[1] = tf32_bits(sm.u2.op.kY[jr][kb] * sjb);
+        mma_tf32(accA, aK, b);
+        mma_tf32(accP, aQ, b);
       }
-      const int r0 = 16 * I + gq, r1 = r0 + 8;
-      uint32_t aK[4], aQ[4];
-      aK[0] = tf32_bits(sm.kX[r0][ka] * cia);
-      aK[1] = tf32_bits(sm.kX[r1][ka] * cia);
-      aK[2] = tf32_bits(sm.kX[r0][kb] * cib);
-      aK[3] = tf32_bits(sm.kX[r1][kb] * cib);
-      aQ[0] = tf32_bits(sm.qX[r0][ka] * cia);
-      aQ[1] = tf32_bits(sm.qX[r1][ka] * cia);
-      aQ[2] = tf32_bits(sm.qX[r0][kb] * cib);
-      aQ[3] = tf32_bits(sm.qX[r1][kb] * cib);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int jr = 16 * J + 8 * nt + gq;
-        uint32_t b[2];
-        b[0] = tf32_bits(sm.kY[jr][ka] * sja);
-        b[1] = tf32_bits(sm.kY[jr][kb] * sjb);
-        mma_tf32(accA[nt], aK, b);
-        mma_tf32(accP[nt], aQ, b);
-      }
-    }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = 16 * I + gq + ((e >> 1) << 3);
         const int j = 16 * J + 8 * nt + 2 * tq + (e & 1);
-        sm.A[i][j] = (j < i) ? sm.beta[i] * accA[nt][e] : 0.f;
-        sm.P[i][j] = (j <= i) ? accP[nt][e] : 0.f;
+        sm.u1.mat.A[i][j] = (j < i) ? sm.beta[i] * accA[e] : 0.f;
+        sm.u1.mat.P[i][j] = (j <= i) ? accP[e] : 0.f;
       }
+    }
+  }
+  // upper blocks of A and P are zero; T starts as zero off the lower blocks
+  for (int x = tid; x < kChunk * kChunk; x += kPrepThreads) {
+    const int i = x / kChunk, j = x % kChunk;
+    if ((j >> 4) > (i >> 4)) {
+      sm.u1.mat.A[i][j] = 0.f;
+      sm.u1.mat.P[i][j] = 0.f;
+      sm.u1.mat.T[i][j] = 0.f;
     }
   }
   __syncthreads();
 
-  // ---- pass 4: T = (I + A)^{-1} by forward substitution (thread per column)
-  for (int i = 0; i < kChunk; ++i) {
-    if (tid < kChunk) {
-      const int col = tid;
-      float t = (i == col) ? 1.f : 0.f;
-      if (col < i) {
-        float acc0 = 0.f, acc1 = 0.f;
-        int j = col;
-        for (; j + 1 < i; j += 2) {
-          acc0 += sm.A[i][j] * sm.Tm[j][col];
-          acc1 += sm.A[i][j + 1] * sm.Tm[j + 1][col];
-        }
-        if (j < i) acc0 += sm.A[i][j] * sm.Tm[j][col];
-        t = -(acc0 + acc1);
+  // ---- pass 4a: diagonal blocks of T by right-looking substitution (thread = (block, column))
+  if (tid < kChunk) {
+    const int J = tid >> 4, col = tid & 15, o = 16 * J;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = (i == col) ? 1.f : 0.f;
+#pragma unroll
+    for (int j = 0; j < 15; ++j) {
+#pragma unroll
+      for (int i = j + 1; i < 16; ++i) x[i] = fmaf(-sm.u1.mat.A[o + i][o + j], x[j], x[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sm.u1.mat.T[o + i][o + col] = x[i];
+  }
+  __syncthreads();
+  // ---- pass 4b: off-diagonal blocks, level d = I - J: Z = sum_{J<=M<I} A_IM T_MJ; T_IJ = -T_II Z
+  for (int d = 1; d < 4; ++d) {
+    const int npairs = 4 - d;
+    for (int x = tid; x < npairs * 256; x += kPrepThreads) {
+      const int J = x >> 8, I = J + d, i = (x >> 4) & 15, col = x & 15;
+      float z = 0.f;
+      for (int M = J; M < I; ++M) {
+#pragma unroll
+        for (int m = 0; m < 16; ++m) z = fmaf(sm.u1.mat.A[16 * I + i][16 * M + m], sm.u1.mat.T[16 * M + m][16 * J + col], z);
       }
-      sm.Tm[i][col] = t;
+      sm.u2.post.Z[J][i][col] = z;
+    }
+    __syncthreads();
+    for (int x = tid; x < npairs * 256; x += kPrepThreads) {
+      const int J = x >> 8, I = J + d, i = (x >> 4) & 15, col = x & 15;
+      float t = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) t = fmaf(sm.u1.mat.T[16 * I + i][16 * I + m], sm.u2.post.Z[J][m][col], t);
+      sm.u1.mat.T[16 * I + i][16 * J + col] = -t;
     }
     __syncthreads();
   }
 
-  // ---- pass 5: M = [-T diag(beta) ; P T diag(beta)] -> fp16, row per thread
+  // ---- pass 5: M = [-T diag(beta) ; P T diag(beta)] in fp16, staged for coalesced stores
   {
-    const int r = tid;  // 0..127
-    __half *dst = p.mats + (((long long)c * p.H + h) * (2 * kChunk) + r) * kChunk;
-    alignas(16) __half rowv[kChunk];
-    if (r < kChunk) {
-#pragma unroll 8
-      for (int j = 0; j < kChunk; ++j) rowv[j] = __float2half_rn(-sm.Tm[r][j] * sm.beta[j]);
-    } else {
-      const int i = r - kChunk;
-      for (int j = 0; j < kChunk; ++j) {
-        float acc = 0.f;
-        for (int m = j; m <= i; ++m) acc += sm.P[i][m] * sm.Tm[m][j];
-        rowv[j] = __float2half_rn(j <= i ? acc * sm.beta[j] : 0.f);
-      }
+    const int i = tid >> 2, jq = tid & 3;   // row i, columns j = jq (mod 4)
+    for (int j = jq; j < kChunk; j += 4) {
+      const float bj = sm.beta[j];
+      sm.u2.post.out[i][j] = __float2half_rn(-sm.u1.mat.T[i][j] * bj);
+      float acc = 0.f;
+      for (int m = j; m <= i; ++m) acc = fmaf(sm.u1.mat.P[i][m], sm.u1.mat.T[m][j], acc);
+      sm.u2.post.out[kChunk + i][j] = __float2half_rn(j <= i ? acc * bj : 0.f);
     }
-    const uint4 *src4 = reinterpret_cast<const uint4 *>(rowv);
-    uint4 *dst4 = reinterpret_cast<uint4 *>(dst);
+  }
+  __syncthreads();
+  {
+    uint4 *dst = reinterpret_cast<uint4 *>(p.mats + ((long long)c * p.H + h) * (2 * kChunk * kChunk));
+    const uint4 *src = reinterpret_cast<const uint4 *>(&sm.u2.post.out[0][0]);
 #pragma unroll
-    for (int x = 0; x < kChunk * 2 / 16; ++x) dst4[x] = src4[x];
+    for (int x = tid; x < 2 * kChunk * kChunk / 8; x += kPrepThreads) dst[x] = src[x];
   }
 }
 

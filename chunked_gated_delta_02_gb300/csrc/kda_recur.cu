@@ -44,7 +44,11 @@ struct RecLayout {
   static constexpr uint32_t kT = Sh + K * 128;                   // 64 x 128  MN-major (A of MMA2)
   static constexpr uint32_t Uh = kT + 2 * kPanel64;              // 64 x 64   MN-major (B of MMA2)
   static constexpr uint32_t qt = Uh + kPanel64;                  // fp32 [64][K]
-  static constexpr uint32_t misc = qt + 64 * K * 4;
+  static constexpr uint32_t rq = qt + 64 * K * 4;               // raw bf16 q, k, g [64][K], v [64][64]
+  static constexpr uint32_t rk = rq + 64 * K * 2;
+  static constexpr uint32_t rg = rk + 64 * K * 2;
+  static constexpr uint32_t rv = rg + 64 * K * 2;
+  static constexpr uint32_t misc = rv + 64 * kBV * 2;
   static constexpr uint32_t bytes = misc + 1024 + 1024;          // + misc + alignment slack
   static_assert(64 * K * 4 <= (K / 64) * 128 * 128, "alpha scratch must fit in WQ");
 };
@@ -63,6 +67,10 @@ recur_tc_kernel(const Problem p) {
                                                         ~static_cast<uintptr_t>(1023));
   float *qt = reinterpret_cast<float *>(sm + Lay::qt);
   float *alpha_s = reinterpret_cast<float *>(sm + Lay::WQ);   // per-channel pass scratch
+  __nv_bfloat16 *rq = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::rq);
+  __nv_bfloat16 *rk = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::rk);
+  __nv_bfloat16 *rg = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::rg);
+  __nv_bfloat16 *rv = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::rv);
   float *kn = reinterpret_cast<float *>(sm + Lay::misc);
   float *qn = kn + 64;
   uint64_t *bar = reinterpret_cast<uint64_t *>(qn + 64);
@@ -133,23 +141,42 @@ recur_tc_kernel(const Problem p) {
     return *s_err == 0;
   };
 
+  // Hand-off matrix of chunk c goes straight into its swizzled K-major operand layout.
+  auto stage_mats = [&](long long c) {
+    const __half *src = p.mats + (c * p.H + h) * (2 * kChunk * kChunk);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int x = tid + kRecThreads * j;   // 16-byte chunk: row x / 8, chunk x % 8
+      cp_async16(sm + Lay::Mh + umma::sw128_chunk(x >> 3, x & 7), src + 8 * x, true);
+    }
+  };
+  if (nch > 0) {
+    const int L0 = min(kChunk, si.len);
+    stage_rows_async<K, kRecThreads>(rq, p.q, p, si.b, si.t0, h, L0, 0, K, tid);
+    stage_rows_async<K, kRecThreads>(rk, p.k, p, si.b, si.t0, h, L0, 0, K, tid);
+    stage_rows_async<K, kRecThreads>(rg, p.g, p, si.b, si.t0, h, L0, 0, K, tid);
+    stage_rows_async<kBV, kRecThreads>(rv, p.v, p, si.b, si.t0, h, L0, v0, p.V, tid);
+    stage_mats(si.chunk0);
+    cp_async_commit();
+  }
+
   bool ok = true;
   for (int n = 0; n < nch && ok; ++n) {
     const int t0 = si.t0 + n * kChunk;
     const int L = min(kChunk, si.len - n * kChunk);
-    const long long cidx = (long long)si.chunk0 + n;
 
-    // ---- A1: row norms; hand-off matrix and v tile into their operand layouts
+    // ---- A1: inputs of this chunk are staged (issued one chunk ahead); row norms; v tile -> fp16 operand
+    cp_async_wait_all();
+    __syncthreads();
     for (int i = warp; i < kChunk; i += kRecThreads / 32) {
       float ssk = 0.f, ssq = 0.f;
-      if (i < L) {
-        const long long row = tok_row(p, si.b, t0 + i, h);
+      const __nv_bfloat162 *kr = reinterpret_cast<const __nv_bfloat162 *>(rk + i * K);
+      const __nv_bfloat162 *qr = reinterpret_cast<const __nv_bfloat162 *>(rq + i * K);
 #pragma unroll
-        for (int kk = lane; kk < K; kk += 32) {
-          const float a = __bfloat162float(p.k[row * K + kk]), b = __bfloat162float(p.q[row * K + kk]);
-          ssk += a * a;
-          ssq += b * b;
-        }
+      for (int x = lane; x < K / 2; x += 32) {
+        const float2 a = __bfloat1622float2(kr[x]), b = __bfloat1622float2(qr[x]);
+        ssk += a.x * a.x + a.y * a.y;
+        ssq += b.x * b.x + b.y * b.y;
       }
       ssk = warp_sum(ssk);
       ssq = warp_sum(ssq);
@@ -158,29 +185,17 @@ recur_tc_kernel(const Problem p) {
         qn[i] = (i < L) ? rsqrtf(ssq + kNormEps) : 0.f;
       }
     }
-    {
-      const uint4 *src = reinterpret_cast<const uint4 *>(p.mats + (cidx * p.H + h) * (2 * kChunk * kChunk));
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int x = tid + kRecThreads * j;   // 16-byte chunk: row x / 8, chunk x % 8
-        *reinterpret_cast<uint4 *>(sm + Lay::Mh + umma::sw128_chunk(x >> 3, x & 7)) = src[x];
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int x = tid + kRecThreads * j;   // v tile: row x / 8, 8 values from column 8 * (x % 8)
-        const int i = x >> 3, c = x & 7;
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (i < L) {
-          const uint4 raw = *reinterpret_cast<const uint4 *>(
-              p.v + tok_row(p, si.b, t0 + i, h) * p.V + v0 + 8 * c);
-          const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-          float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]);
-          float2 f2 = __bfloat1622float2(b2[2]), f3 = __bfloat1622float2(b2[3]);
-          w = make_uint4(pack_half2(f0.x, f0.y), pack_half2(f1.x, f1.y), pack_half2(f2.x, f2.y),
-                         pack_half2(f3.x, f3.y));
-        }
-        *reinterpret_cast<uint4 *>(sm + Lay::vh + umma::sw128_chunk(i, c)) = w;
-      }
+    for (int j = 0; j < 4; ++j) {
+      const int x = tid + kRecThreads * j;   // v tile: row x / 8, 8 values from column 8 * (x % 8)
+      const int i = x >> 3, cc = x & 7;
+      const uint4 raw = *reinterpret_cast<const uint4 *>(rv + i * kBV + 8 * cc);
+      const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+      const float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]);
+      const float2 f2 = __bfloat1622float2(b2[2]), f3 = __bfloat1622float2(b2[3]);
+      *reinterpret_cast<uint4 *>(sm + Lay::vh + umma::sw128_chunk(i, cc)) =
+          make_uint4(pack_half2(f0.x, f0.y), pack_half2(f1.x, f1.y), pack_half2(f2.x, f2.y),
+                     pack_half2(f3.x, f3.y));
     }
     __syncthreads();
 
@@ -190,14 +205,11 @@ recur_tc_kernel(const Problem p) {
       const uint32_t col_off = (uint32_t)(kk >> 6) * Lay::kPanel64;
       float Gam = 1.f;
       for (int i = 0; i < kChunk; ++i) {
-        float kv = 0.f, qv = 0.f, al = 1.f;
-        if (i < L) {
-          const long long row = tok_row(p, si.b, t0 + i, h);
-          al = ex2_approx(log2_decay(__bfloat162float(p.g[row * K + kk]), dt, ea, lbl2));
-          kv = __bfloat162float(p.k[row * K + kk]) * kn[i];
-          qv = __bfloat162float(p.q[row * K + kk]) * qn[i];
-          Gam *= al;
-        }
+        float al = 1.f;
+        if (i < L) al = ex2_approx(log2_decay(__bfloat162float(rg[i * K + kk]), dt, ea, lbl2));
+        const float kv = __bfloat162float(rk[i * K + kk]) * kn[i];
+        const float qv = __bfloat162float(rq[i * K + kk]) * qn[i];
+        Gam *= al;
         alpha_s[i * K + kk] = al;
         *reinterpret_cast<__half *>(sm + Lay::kG + col_off + umma::sw128_offset(i, kk & 63)) =
             __float2half_rn(kv * Gam);
@@ -206,12 +218,21 @@ recur_tc_kernel(const Problem p) {
       gam = Gam;
       float suf = 1.f;
       for (int i = kChunk - 1; i >= 0; --i) {
-        float kv = 0.f;
-        if (i < L) kv = __bfloat162float(p.k[tok_row(p, si.b, t0 + i, h) * K + kk]) * kn[i];
+        const float kv = __bfloat162float(rk[i * K + kk]) * kn[i];
         *reinterpret_cast<__half *>(sm + Lay::kT + col_off + umma::sw128_offset(i, kk & 63)) =
             __float2half_rn(kv * suf);
         suf *= alpha_s[i * K + kk];
       }
+    }
+    __syncthreads();
+    // raw q, k, g, v of this chunk are consumed: prefetch the next chunk's
+    if (n + 1 < nch) {
+      const int t1 = t0 + kChunk, L1 = min(kChunk, si.len - (n + 1) * kChunk);
+      stage_rows_async<K, kRecThreads>(rq, p.q, p, si.b, t1, h, L1, 0, K, tid);
+      stage_rows_async<K, kRecThreads>(rk, p.k, p, si.b, t1, h, L1, 0, K, tid);
+      stage_rows_async<K, kRecThreads>(rg, p.g, p, si.b, t1, h, L1, 0, K, tid);
+      stage_rows_async<kBV, kRecThreads>(rv, p.v, p, si.b, t1, h, L1, v0, p.V, tid);
+      cp_async_commit();
     }
     umma::fence_proxy_async_smem();
     umma::fence_before_sync();
@@ -230,6 +251,10 @@ recur_tc_kernel(const Problem p) {
       umma::commit(bar);
     }
     if (!(ok = wait_mma())) break;
+    if (n + 1 < nch) {   // M is consumed by D1/D2: prefetch the next chunk's
+      stage_mats((long long)si.chunk0 + n + 1);
+      cp_async_commit();
+    }
 
     // ---- C: WQ rows: w = -D1 (rows < 64), Q' = q~ - D1 (rows >= 64)
 #pragma unroll 1
@@ -343,6 +368,7 @@ recur_tc_kernel(const Problem p) {
     __syncthreads();
   }
 
+  cp_async_wait_all();
   if (!ok) {
     if (tid == 0) atomicExch(p.dev_status, kDevWaitTimeout);
     // one more bounded wait (on the phase that timed out) so that no MMA of
