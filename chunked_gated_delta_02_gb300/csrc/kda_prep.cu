@@ -41,7 +41,7 @@ constexpr int kPrepThreads = 256;
 template <int K>
 struct PrepSmem {
   static constexpr int KF = K + 4;   // fp32 row stride (floats)
-  static constexpr int LD = kChunk + 1;
+  static constexpr int LD = kChunk + 4;   // row stride = 4 (mod 32) words: conflict-free A fragments
   union {
     struct {                          // passes 0-2: raw staged inputs
       __nv_bfloat16 q[kChunk * K], k[kChunk * K], g[kChunk * K];
@@ -57,7 +57,7 @@ struct PrepSmem {
     } op;
     struct {                          // passes 4-5
       float Z[3][16][17];
-      __half out[2 * kChunk][kChunk];
+      __half out[2 * kChunk][kChunk + 8];    // padded rows: conflict-free fragment stores
     } post;
   } u2;
   float Bs[4][K];                     // whole-block log2 decay B_J
@@ -245,23 +245,53 @@ prep_kernel(const Problem p) {
     __syncthreads();
   }
 
-  // ---- pass 5: M = [-T diag(beta) ; P T diag(beta)] in fp16, staged for coalesced stores
+  // ---- pass 5: M = [-T diag(beta) ; P T diag(beta)] in fp16, staged for coalesced stores.
+  // P T on the tensor cores: output tile (16-row mt, 8-col nt); P is lower, T lower, so only
+  // tiles with 8 nt <= 16 mt + 15 are non-zero and their k range is [8 nt, 16 mt + 16).
   {
-    const int i = tid >> 2, jq = tid & 3;   // row i, columns j = jq (mod 4)
-    for (int j = jq; j < kChunk; j += 4) {
-      const float bj = sm.beta[j];
-      sm.u2.post.out[i][j] = __float2half_rn(-sm.u1.mat.T[i][j] * bj);
-      float acc = 0.f;
-      for (int m = j; m <= i; ++m) acc = fmaf(sm.u1.mat.P[i][m], sm.u1.mat.T[m][j], acc);
-      sm.u2.post.out[kChunk + i][j] = __float2half_rn(j <= i ? acc * bj : 0.f);
+    const int gq = lane >> 2, tq = lane & 3;
+    for (int item = warp; item < 20; item += kPrepThreads / 32) {
+      int mt = 0;
+      while (item >= (mt + 1) * (mt + 2)) ++mt;   // items per mt: 2, 4, 6, 8
+      const int nt = item - mt * (mt + 1);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int ks = nt; ks <= 2 * mt + 1; ++ks) {
+        uint32_t a[4], b[2];
+        const int r0 = 16 * mt + gq, c0 = 8 * ks + tq;
+        a[0] = tf32_bits(sm.u1.mat.P[r0][c0]);
+        a[1] = tf32_bits(sm.u1.mat.P[r0 + 8][c0]);
+        a[2] = tf32_bits(sm.u1.mat.P[r0][c0 + 4]);
+        a[3] = tf32_bits(sm.u1.mat.P[r0 + 8][c0 + 4]);
+        b[0] = tf32_bits(sm.u1.mat.T[8 * ks + tq][8 * nt + gq]);
+        b[1] = tf32_bits(sm.u1.mat.T[8 * ks + tq + 4][8 * nt + gq]);
+        mma_tf32(acc, a, b);
+      }
+      const int j0 = 8 * nt + 2 * tq;
+      const float b0 = sm.beta[j0], b1 = sm.beta[j0 + 1];
+#pragma unroll
+      for (int hrow = 0; hrow < 2; ++hrow) {
+        const int i = 16 * mt + gq + 8 * hrow;
+        *reinterpret_cast<__half2 *>(&sm.u2.post.out[kChunk + i][j0]) =
+            __floats2half2_rn(j0 <= i ? acc[2 * hrow] * b0 : 0.f, j0 + 1 <= i ? acc[2 * hrow + 1] * b1 : 0.f);
+      }
+    }
+    // zero tiles of P T (above the block diagonal) and the -T diag(beta) half
+    for (int x = tid; x < kChunk * kChunk / 2; x += kPrepThreads) {
+      const int i = x / (kChunk / 2), j = 2 * (x % (kChunk / 2));
+      *reinterpret_cast<__half2 *>(&sm.u2.post.out[i][j]) =
+          __floats2half2_rn(-sm.u1.mat.T[i][j] * sm.beta[j], -sm.u1.mat.T[i][j + 1] * sm.beta[j + 1]);
+      if ((j >> 3) > 2 * (i >> 4) + 1)
+        *reinterpret_cast<__half2 *>(&sm.u2.post.out[kChunk + i][j]) = __floats2half2_rn(0.f, 0.f);
     }
   }
   __syncthreads();
   {
     uint4 *dst = reinterpret_cast<uint4 *>(p.mats + ((long long)c * p.H + h) * (2 * kChunk * kChunk));
-    const uint4 *src = reinterpret_cast<const uint4 *>(&sm.u2.post.out[0][0]);
 #pragma unroll
-    for (int x = tid; x < 2 * kChunk * kChunk / 8; x += kPrepThreads) dst[x] = src[x];
+    for (int x = tid; x < 2 * kChunk * kChunk / 8; x += kPrepThreads) {
+      const int r = x >> 3, cc = x & 7;
+      dst[x] = *reinterpret_cast<const uint4 *>(&sm.u2.post.out[r][8 * cc]);
+    }
   }
 }
 
