@@ -1,8 +1,11 @@
 // Host side of the C ABI declared in include/kda.h: argument validation,
 // workspace layout, and the K0 -> K1 -> K2 launch sequence on one stream.
+#include <cudaTypedefs.h>
+
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/kda.h"
 #include "kda_common.cuh"
@@ -10,7 +13,7 @@
 namespace kda {
 cudaError_t launch_varlen_schedule(const Problem &p, cudaStream_t stream);
 cudaError_t launch_prep(const Problem &p, cudaStream_t stream);
-cudaError_t launch_recur(const Problem &p, cudaStream_t stream);
+cudaError_t launch_recur(const Problem &p, const TmaMaps &maps, cudaStream_t stream);
 }  // namespace kda
 
 // Sticky per-device data-error word (KDA_DEVICE_* codes).
@@ -24,7 +27,7 @@ constexpr size_t kMatBytes = 2ull * kda::kChunk * kda::kChunk * sizeof(__half); 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t flag_off, chunk_off_off, order_off, mats_off, total;
+  size_t flag_off, chunk_off_off, order_off, mats_off, la2_off, total;
 };
 
 bool sizes_ok(int B, int T, int H, int K, int V, int N) {
@@ -35,7 +38,7 @@ int64_t max_chunks_of(int B, int T, int N) {
   return (int64_t)B * ((T + kda::kChunk - 1) / kda::kChunk) + (int64_t)N;
 }
 
-Layout layout_of(int B, int T, int H, int N) {
+Layout layout_of(int B, int T, int H, int K, int N) {
   Layout L;
   size_t off = 0;
   L.flag_off = off;
@@ -46,11 +49,44 @@ Layout layout_of(int B, int T, int H, int N) {
   off = align_up(off + sizeof(int32_t) * ((size_t)N + 1));
   L.mats_off = off;
   off = align_up(off + (size_t)max_chunks_of(B, T, N) * (size_t)H * kMatBytes);
+  L.la2_off = off;
+  off = align_up(off + (size_t)B * (size_t)T * (size_t)H * (size_t)K * sizeof(__half));
   L.total = off;
   return L;
 }
 
 bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// 4D view [B][T][H][D] of a 16-bit token tensor, box = (box_d, 1, 64, 1).
+bool encode_token_map(CUtensorMap *m, const void *base, int D, int H, int T, int B, int box_d,
+                      CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)T * H * D * 2};
+  const cuuint32_t box[4] = {(cuuint32_t)box_d, 1, (cuuint32_t)kda::kChunk, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, dtype, 4, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 kda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
@@ -127,6 +163,7 @@ kda_status_t fill_problem(kda::Problem &p, const Layout &L, void *ws, const void
   p.chunk_off = reinterpret_cast<int32_t *>(base + L.chunk_off_off);
   p.order = reinterpret_cast<int32_t *>(base + L.order_off);
   p.mats = reinterpret_cast<__half *>(base + L.mats_off);
+  p.la2 = reinterpret_cast<__half *>(base + L.la2_off);
   if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p.dev_status), g_kda_device_status) != cudaSuccess) {
     cudaGetLastError();
     return KDA_ERR_CUDA;
@@ -157,7 +194,7 @@ int64_t kda_max_chunks(int B, int T, int num_seqs) {
 
 size_t kda_fwd_workspace_size(int B, int T, int H, int K, int V, int num_seqs) {
   if (!sizes_ok(B, T, H, K, V, num_seqs)) return 0;
-  return layout_of(B, T, H, num_seqs).total;
+  return layout_of(B, T, H, K, num_seqs).total;
 }
 
 const char *kda_status_string(kda_status_t s) {
@@ -202,7 +239,7 @@ kda_status_t kda_fwd_with_events(const void *q, const void *k, const void *v, co
     return KDA_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (num_seqs == 0) return KDA_OK;
-  const Layout L = layout_of(B, T, H, num_seqs);
+  const Layout L = layout_of(B, T, H, K, num_seqs);
   Scratch scr;
   st = get_scratch(workspace, workspace_bytes, L.total, s, scr);
   if (st != KDA_OK) return st;
@@ -216,7 +253,14 @@ kda_status_t kda_fwd_with_events(const void *q, const void *k, const void *v, co
   if (st == KDA_OK && cu_seqlens) st = from_cuda(kda::launch_varlen_schedule(p, s));
   if (st == KDA_OK) st = from_cuda(kda::launch_prep(p, s));
   mark(events ? events->prep_done : nullptr);
-  if (st == KDA_OK) st = from_cuda(kda::launch_recur(p, s));
+  kda::TmaMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  if (st == KDA_OK && T > 0 &&
+      !(encode_token_map(&maps.q, q, K, H, T, B, K) && encode_token_map(&maps.k, k, K, H, T, B, K) &&
+        encode_token_map(&maps.la2, p.la2, K, H, T, B, K, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) &&
+        encode_token_map(&maps.v, v, V, H, T, B, 64)))
+    st = KDA_ERR_CUDA;
+  if (st == KDA_OK) st = from_cuda(kda::launch_recur(p, maps, s));
   mark(events ? events->recur_done : nullptr);
   release_scratch(scr, s);
   return st;
@@ -243,7 +287,7 @@ kda_status_t kda_debug_chunk_matrices(const void *q, const void *k, const void *
   if (!chunk_mats || !aligned(chunk_mats, 16)) return KDA_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (num_seqs == 0) return KDA_OK;
-  const Layout L = layout_of(B, T, H, num_seqs);
+  const Layout L = layout_of(B, T, H, K, num_seqs);
   Scratch scr;
   st = get_scratch(workspace, workspace_bytes, L.total, s, scr);
   if (st != KDA_OK) return st;

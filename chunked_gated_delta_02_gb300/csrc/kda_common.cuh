@@ -7,6 +7,7 @@
 // same base-2 exponential trick).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -31,6 +32,7 @@ struct Problem {
   const int32_t *cu;                 // [N+1] or null (fixed length)
   __nv_bfloat16 *o;                  // [B,T,H,V]
   __half *mats;                      // [max_chunks][H][2C][C] fp16 hand-off
+  __half *la2;                       // [B,T,H,K] fp16 per-token base-2 log decay (prep -> recurrence)
   int32_t *chunk_off;                // [N+1] varlen chunk offsets (K0 output)
   int32_t *order;                    // [N] varlen longest-first order (K0 output)
   int32_t *flag;                     // per-call data-error flag (varlen) or null
@@ -39,6 +41,14 @@ struct Problem {
   int B, T, H, K, V, N;
   int nc_fixed;                      // ceil(T / C) in fixed-length mode
   long long max_chunks;
+};
+
+// TMA descriptors of the token tensors (q, k, the fp16 log-decay la2, v), viewed as
+// 4D [B][T][H][D] (innermost D)
+// with a box of (D or 64 columns) x 1 head x 64 tokens x 1 batch row: one copy per
+// chunk and tensor; tokens past T read as zeros.
+struct TmaMaps {
+  CUtensorMap q, k, la2, v;
 };
 
 struct SeqInfo {

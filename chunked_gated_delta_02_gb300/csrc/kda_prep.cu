@@ -5,7 +5,8 @@
 // gate activation, L2 normalisation, decay, and the triangular inverse, all
 // parallel over tokens) and the cuLA "kda chunk intra" stage (cuLA launch
 // blog, section "Status & Roadmap"), and hands the recurrence kernel one
-// 128 x 64 fp16 matrix per (chunk, head):
+// 128 x 64 fp16 matrix per (chunk, head), stored in the 128-byte-swizzled row
+// order of its shared-memory operand image (so one bulk copy places it):
 //
 //   M = [ -Tb ; P Tb ],   Tb = (I + A)^{-1} diag(beta)
 //   A_ij = beta_i sum_k khat_ik khat_jk 2^{G_ik - G_jk}   (j < i)
@@ -36,7 +37,7 @@
 
 namespace kda {
 
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 512;
 
 template <int K>
 struct PrepSmem {
@@ -127,17 +128,20 @@ prep_kernel(const Problem p) {
   {
     const float ea = expf(p.A_log[h]);
     const float lbl2 = p.lb * kLog2e;
-    constexpr int kBlocksPerThread = 4 * K / kPrepThreads;   // 2 for K=128, 1 for K=64
-    const int kk = tid % K;
-    const float dt = p.dt_bias ? p.dt_bias[h * K + kk] : 0.f;
-#pragma unroll
-    for (int bj = 0; bj < kBlocksPerThread; ++bj) {
-      const int J = (tid / K) * kBlocksPerThread + bj;
+    for (int unit = tid; unit < 4 * K; unit += kPrepThreads) {
+      const int kk = unit % K, J = unit / K;
+      const float dt = p.dt_bias ? p.dt_bias[h * K + kk] : 0.f;
       float Gb = 0.f;
 #pragma unroll 4
       for (int r = 0; r < 16; ++r) {
         const int i = 16 * J + r;
-        if (i < len) Gb += log2_decay(__bfloat162float(sm.u1.raw.g[i * K + kk]), dt, ea, lbl2);
+        if (i < len) {
+          // the log decay is rounded to fp16 once; this kernel and the recurrence kernel both use
+          // the rounded value, so the two stay consistent
+          const __half la = __float2half_rn(log2_decay(__bfloat162float(sm.u1.raw.g[i * K + kk]), dt, ea, lbl2));
+          p.la2[tok_row(p, si.b, t0 + i, h) * K + kk] = la;
+          Gb += __half2float(la);
+        }
         const float kv = __bfloat162float(sm.u1.raw.k[i * K + kk]) * sm.kn[i];
         const float qv = __bfloat162float(sm.u1.raw.q[i * K + kk]) * sm.qn[i];
         const float X = ex2_approx(Gb), Y = ex2_approx(-Gb);
@@ -289,8 +293,10 @@ prep_kernel(const Problem p) {
     uint4 *dst = reinterpret_cast<uint4 *>(p.mats + ((long long)c * p.H + h) * (2 * kChunk * kChunk));
 #pragma unroll
     for (int x = tid; x < 2 * kChunk * kChunk / 8; x += kPrepThreads) {
+      // stored as the 128-byte-swizzled shared-memory image of the K-major operand:
+      // 16-byte chunk cc of row r at position r * 8 + (cc ^ (r & 7))
       const int r = x >> 3, cc = x & 7;
-      dst[x] = *reinterpret_cast<const uint4 *>(&sm.u2.post.out[r][8 * cc]);
+      dst[r * 8 + (cc ^ (r & 7))] = *reinterpret_cast<const uint4 *>(&sm.u2.post.out[r][8 * cc]);
     }
   }
 }

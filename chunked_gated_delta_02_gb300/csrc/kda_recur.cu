@@ -55,7 +55,7 @@ struct RecLayout {
   static constexpr uint32_t kT = Sh + K * 128;                   // 64 x 128  MN-major (A of MMA2)
   static constexpr uint32_t Uh = kT + 2 * kPanel64;              // 64 x 64   MN-major (B of MMA2)
   static constexpr uint32_t qt = Uh + kPanel64;                  // fp16 [64][K] plain
-  static constexpr uint32_t rq = qt + 64 * K * 2;                // raw bf16 q, k, g [64][K], v [64][64]
+  static constexpr uint32_t rq = qt + 64 * K * 2;                // raw bf16 q, k, fp16 la2 [64][K], bf16 v [64][64]
   static constexpr uint32_t rk = rq + 64 * K * 2;
   static constexpr uint32_t rg = rk + 64 * K * 2;
   static constexpr uint32_t rv = rg + 64 * K * 2;
@@ -66,7 +66,7 @@ struct RecLayout {
 // Small per-CTA state after the operand buffers.
 template <int K>
 struct RecMisc {
-  uint64_t bar_d12, bar_wq_full, bar_mma1, bar_mma2, bar_exit;
+  uint64_t bar_d12, bar_wq_full, bar_mma1, bar_mma2, bar_exit, bar_in, bar_m;
   uint32_t tmem_slot;
   int err;
   float kn[kChunk], qn[kChunk];
@@ -81,7 +81,7 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
 
 template <int K>
 __global__ void __launch_bounds__(kRecThreads, 1)
-recur_tc_kernel(const Problem p) {
+recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   using Lay = RecLayout<K>;
   constexpr int CPT = K / 64;   // channels per prep thread
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -121,6 +121,8 @@ recur_tc_kernel(const Problem p) {
     umma::mbar_init(&ms.bar_mma1, 1);
     umma::mbar_init(&ms.bar_mma2, 1);
     umma::mbar_init(&ms.bar_exit, 2);
+    umma::mbar_init(&ms.bar_in, 1);
+    umma::mbar_init(&ms.bar_m, 1);
     umma::mbar_fence_init();
     ms.err = 0;
   }
@@ -140,34 +142,40 @@ recur_tc_kernel(const Problem p) {
       *reinterpret_cast<uint4 *>(sm + Lay::Sh + umma::sw128_chunk(tid, c)) = w;
     }
   }
+  // Inputs of chunk n: one tiled TMA copy per tensor (q, k, g: 64 x K; v: 64 x 64 at column v0),
+  // issued by one prep thread and completing on bar_in. Tokens past T read as zeros; tokens of
+  // the next packed sequence are zeroed after arrival.
   auto stage_inputs = [&](int n) {
-    const int tn = si.t0 + n * kChunk, Ln = min(kChunk, si.len - n * kChunk);
-    stage_rows_async<K, kPrepGroupThreads>(rq, p.q, p, si.b, tn, h, Ln, 0, K, pt);
-    stage_rows_async<K, kPrepGroupThreads>(rk, p.k, p, si.b, tn, h, Ln, 0, K, pt);
-    stage_rows_async<K, kPrepGroupThreads>(rg, p.g, p, si.b, tn, h, Ln, 0, K, pt);
-    stage_rows_async<kBV, kPrepGroupThreads>(rv, p.v, p, si.b, tn, h, Ln, v0, p.V, pt);
-  };
-  auto stage_mats = [&](int n) {   // hand-off matrix straight into its swizzled K-major layout
-    const __half *src = p.mats + (((long long)si.chunk0 + n) * p.H + h) * (2 * kChunk * kChunk);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int x = pt + kPrepGroupThreads * j;   // 16-byte chunk: row x / 8, chunk x % 8
-      cp_async16(sm + Lay::Mh + umma::sw128_chunk(x >> 3, x & 7), src + 8 * x, true);
+    if (pt == 0) {
+      const int tn = si.t0 + n * kChunk;
+      umma::mbar_arrive_expect_tx(&ms.bar_in, (uint32_t)kChunk * (3 * K * 2 + kBV * 2));
+      umma::tma_load_4d(rq, &maps.q, 0, h, tn, si.b, &ms.bar_in);
+      umma::tma_load_4d(rk, &maps.k, 0, h, tn, si.b, &ms.bar_in);
+      umma::tma_load_4d(rg, &maps.la2, 0, h, tn, si.b, &ms.bar_in);
+      umma::tma_load_4d(rv, &maps.v, v0, h, tn, si.b, &ms.bar_in);
     }
   };
-  if (!is_chain && nch > 0) {
-    stage_inputs(0);
-    stage_mats(0);
-    cp_async_commit();
-  }
+  // Hand-off matrix of chunk n: stored pre-swizzled, so one 16 KB bulk copy places it.
+  auto stage_mats = [&](int n) {
+    if (pt == 0) {
+      umma::mbar_arrive_expect_tx(&ms.bar_m, 2 * kChunk * kChunk * 2);
+      umma::bulk_g2s(sm + Lay::Mh, p.mats + (((long long)si.chunk0 + n) * p.H + h) * (2 * kChunk * kChunk),
+                     2 * kChunk * kChunk * 2, &ms.bar_m);
+    }
+  };
   umma::fence_proxy_async_smem();
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
+  if (!is_chain && nch > 0) {
+    stage_inputs(0);
+    stage_mats(0);
+  }
   const uint32_t tmem = ms.tmem_slot;
   const uint32_t tD1 = tmem, tD3 = tmem + 256;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   bool bad = false;   // this thread saw a wait time out
+  uint32_t in_done = 0, m_done = 0;   // completed bar_in / bar_m phases seen by this thread
 
   auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
     if (bad) return;
@@ -267,20 +275,26 @@ recur_tc_kernel(const Problem p) {
     }
   } else {
     // ======================= prep group =======================
-    const float ea = expf(p.A_log[h]);
-    const float lbl2 = p.lb * kLog2e;
     const int cg = pt % 64, J = pt / 64;          // channels [cg*CPT, cg*CPT+CPT), rows [16J, 16J+16)
-    float dtv[CPT];
-#pragma unroll
-    for (int e = 0; e < CPT; ++e) dtv[e] = p.dt_bias ? p.dt_bias[h * K + cg * CPT + e] : 0.f;
     const uint32_t col_panel = (uint32_t)((cg * CPT) >> 6) * Lay::kPanel64;
     const int col_in = (cg * CPT) & 63;
     for (int n = 0; n < nch; ++n) {
-      cp_async_wait_all();
-      if (umma::bar_red_or(kBarPrep, kPrepGroupThreads, bad || *(volatile int *)&ms.err != 0)) break;
       const uint32_t par = (uint32_t)(n & 1);
       const uint32_t tD2 = tmem + 128 + 64 * (n & 1);
       const int L = min(kChunk, si.len - n * kChunk);
+      wait_bar(&ms.bar_in, par);
+      in_done += bad ? 0u : 1u;
+      if (L < kChunk) {   // rows past the sequence end (next packed sequence or zero fill): zero them
+        for (int x = pt; x < (kChunk - L) * (3 * K + kBV) / 8; x += kPrepGroupThreads) {
+          const int per_row = (3 * K + kBV) / 8, i = L + x / per_row, c = x % per_row;
+          __nv_bfloat16 *dst = (c < K / 8) ? rq + i * K + 8 * c
+                               : (c < 2 * K / 8) ? rk + i * K + 8 * (c - K / 8)
+                               : (c < 3 * K / 8) ? rg + i * K + 8 * (c - 2 * K / 8)
+                                                 : rv + i * kBV + 8 * (c - 3 * K / 8);
+          *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (umma::bar_red_or(kBarPrep, kPrepGroupThreads, bad || *(volatile int *)&ms.err != 0)) break;
       // -- row norms: 4 threads per row, K/4 channels each (bf16x2 from the staged rows)
       {
         const int row = pt >> 2, qd = pt & 3;
@@ -315,72 +329,86 @@ recur_tc_kernel(const Problem p) {
             make_uint4(pack_half2(f0.x, f0.y), pack_half2(f1.x, f1.y), pack_half2(f2.x, f2.y),
                        pack_half2(f3.x, f3.y));
       }
-      // -- gate: per-token decays alpha of this thread's 16 rows, and their product over the block
-      float al[16][CPT];
-      float bt[CPT];
+      // -- per-token decays alpha = 2^la2 of this thread's 16 rows (la2 from the prep kernel)
+      //    and their product over the block (two channels per thread, packed f32x2 arithmetic)
+      float2 al[16], bt = make_float2(1.f, 1.f), pre, suf, kts[16];
+      {
+        const __half *lr = reinterpret_cast<const __half *>(rg);
+        const float2 one = make_float2(1.f, 1.f);
 #pragma unroll
-      for (int e = 0; e < CPT; ++e) bt[e] = 1.f;
-#pragma unroll
-      for (int rr = 0; rr < 16; ++rr) {
-        const int i = 16 * J + rr;
-#pragma unroll
-        for (int e = 0; e < CPT; ++e) {
-          const float gv = __bfloat162float(rg[i * K + cg * CPT + e]);
-          al[rr][e] = (i < L) ? ex2_approx(log2_decay(gv, dtv[e], ea, lbl2)) : 1.f;
-          bt[e] *= al[rr][e];
+        for (int rr = 0; rr < 16; ++rr) {
+          const int i = 16 * J + rr;
+          float2 la;
+          if constexpr (CPT == 2) la = __half22float2(*reinterpret_cast<const __half2 *>(lr + i * K + 2 * cg));
+          else la = make_float2(__half2float(lr[i * K + cg]), 0.f);
+          al[rr] = (i < L) ? make_float2(ex2_approx(la.x), ex2_approx(la.y)) : one;
+          bt = __fmul2_rn(bt, al[rr]);
         }
       }
-#pragma unroll
-      for (int e = 0; e < CPT; ++e) ms.btot[J][cg * CPT + e] = bt[e];
+      ms.btot[J][cg * CPT] = bt.x;
+      if constexpr (CPT == 2) ms.btot[J][cg * CPT + 1] = bt.y;
       umma::named_bar(kBarPrep, kPrepGroupThreads);   // norms, block products visible
       // -- decayed operands: kG = khat Gamma and q~ = qhat Gamma (forward), k~ = khat Gamma_last / Gamma
-      float pre[CPT], suf[CPT];
+      {
+        float a[2] = {1.f, 1.f}, b[2] = {1.f, 1.f};
 #pragma unroll
-      for (int e = 0; e < CPT; ++e) {
-        const int c = cg * CPT + e;
-        float a = 1.f, b = 1.f;
+        for (int e = 0; e < CPT; ++e) {
+          const int c = cg * CPT + e;
 #pragma unroll
-        for (int M = 0; M < 4; ++M) {
-          if (M < J) a *= ms.btot[M][c];
-          if (M > J) b *= ms.btot[M][c];
+          for (int M = 0; M < 4; ++M) {
+            if (M < J) a[e] *= ms.btot[M][c];
+            if (M > J) b[e] *= ms.btot[M][c];
+          }
         }
-        pre[e] = a;
-        suf[e] = b;
-        if (J == 0) ms.gam[n & 1][c] = a * bt[e] * b;
+        pre = make_float2(a[0], a[1]);
+        suf = make_float2(b[0], b[1]);
+        if (J == 0) {
+          ms.gam[n & 1][cg * CPT] = a[0] * bt.x * b[0];
+          if constexpr (CPT == 2) ms.gam[n & 1][cg * CPT + 1] = a[1] * bt.y * b[1];
+        }
       }
 #pragma unroll
       for (int rr = 0; rr < 16; ++rr) {
         const int i = 16 * J + rr;
-        float kgv[CPT], qtv[CPT];
-#pragma unroll
-        for (int e = 0; e < CPT; ++e) {
-          pre[e] *= al[rr][e];
-          kgv[e] = __bfloat162float(rk[i * K + cg * CPT + e]) * ms.kn[i] * pre[e];
-          qtv[e] = __bfloat162float(rq[i * K + cg * CPT + e]) * ms.qn[i] * pre[e];
+        float2 kv, qv;
+        if constexpr (CPT == 2) {
+          kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(rk + i * K + 2 * cg));
+          qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(rq + i * K + 2 * cg));
+        } else {
+          kv = make_float2(__bfloat162float(rk[i * K + cg]), 0.f);
+          qv = make_float2(__bfloat162float(rq[i * K + cg]), 0.f);
         }
+        const float kn = ms.kn[i], qn = ms.qn[i];
+        pre = __fmul2_rn(pre, al[rr]);
+        const float2 kg = __fmul2_rn(kv, __fmul2_rn(pre, make_float2(kn, kn)));
+        const float2 qq = __fmul2_rn(qv, __fmul2_rn(pre, make_float2(qn, qn)));
         if constexpr (CPT == 2) {
           *reinterpret_cast<uint32_t *>(sm + Lay::kG + col_panel + umma::sw128_offset(i, col_in)) =
-              pack_half2(kgv[0], kgv[1]);
-          *reinterpret_cast<uint32_t *>(qt + i * K + cg * CPT) = pack_half2(qtv[0], qtv[1]);
+              pack_half2(kg.x, kg.y);
+          *reinterpret_cast<uint32_t *>(qt + i * K + cg * CPT) = pack_half2(qq.x, qq.y);
         } else {
           *reinterpret_cast<__half *>(sm + Lay::kG + col_panel + umma::sw128_offset(i, col_in)) =
-              __float2half_rn(kgv[0]);
-          qt[i * K + cg * CPT] = __float2half_rn(qtv[0]);
+              __float2half_rn(kg.x);
+          qt[i * K + cg * CPT] = __float2half_rn(qq.x);
         }
       }
-      float kts[16][CPT];
 #pragma unroll
       for (int rr = 15; rr >= 0; --rr) {
         const int i = 16 * J + rr;
-#pragma unroll
-        for (int e = 0; e < CPT; ++e) {
-          kts[rr][e] = __bfloat162float(rk[i * K + cg * CPT + e]) * ms.kn[i] * suf[e];
-          suf[e] *= al[rr][e];
-        }
+        float2 kv;
+        if constexpr (CPT == 2) kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(rk + i * K + 2 * cg));
+        else kv = make_float2(__bfloat162float(rk[i * K + cg]), 0.f);
+        const float kn = ms.kn[i];
+        kts[rr] = __fmul2_rn(kv, __fmul2_rn(suf, make_float2(kn, kn)));
+        suf = __fmul2_rn(suf, al[rr]);
       }
       umma::fence_proxy_async_smem();
       umma::fence_before_sync();
       umma::named_bar(kBarPrep, kPrepGroupThreads);   // kG, vh, qt complete; raw inputs consumed
+      if (pt == 0) {
+        wait_bar(&ms.bar_m, par);
+        m_done += bad ? 0u : 1u;
+      }
       if (pt == 0 && !bad) {   // D1 = M (khat Gamma), D2 = M v
         umma::fence_after_sync();
         const uint32_t id1 = umma::idesc_f16(128, K, 0, 1), id2 = umma::idesc_f16(128, kBV, 0, 1);
@@ -394,15 +422,10 @@ recur_tc_kernel(const Problem p) {
         }
         umma::commit(&ms.bar_d12);
       }
-      if (n + 1 < nch) {   // raw inputs of chunk n are consumed: stage chunk n+1
-        stage_inputs(n + 1);
-        cp_async_commit();
-      }
+      if (n + 1 < nch) stage_inputs(n + 1);   // raw inputs of chunk n are consumed
       wait_bar(&ms.bar_d12, par);
-      if (n + 1 < nch) {   // M is consumed by D1/D2: stage chunk n+1's
-        stage_mats(n + 1);
-        cp_async_commit();
-      }
+      if (n + 1 < nch) stage_mats(n + 1);                 // M is consumed by D1/D2
+
       // -- WQ rows: w = -D1 (rows < 64), Q' = q~ - D1 (rows >= 64); WQ must be free (MMA1 of n-1 done)
       if (n > 0) wait_bar(&ms.bar_mma1, par ^ 1u);
       {
@@ -444,10 +467,10 @@ recur_tc_kernel(const Problem p) {
         const int i = 16 * J + rr;
         if constexpr (CPT == 2) {
           *reinterpret_cast<uint32_t *>(sm + Lay::kT + col_panel + umma::sw128_offset(i, col_in)) =
-              pack_half2(kts[rr][0], kts[rr][1]);
+              pack_half2(kts[rr].x, kts[rr].y);
         } else {
           *reinterpret_cast<__half *>(sm + Lay::kT + col_panel + umma::sw128_offset(i, col_in)) =
-              __float2half_rn(kts[rr][0]);
+              __float2half_rn(kts[rr].x);
         }
       }
       umma::fence_proxy_async_smem();
@@ -457,10 +480,17 @@ recur_tc_kernel(const Problem p) {
     }
   }
 
-  // ---- exit: no cp.async or tensor-core work of this CTA may be in flight past this point
-  cp_async_wait_all();
+  // ---- exit: no bulk copy or tensor-core work of this CTA may be in flight past this point.
+  // On a normal exit every copy was waited for; after a timeout, wait (bounded) for the
+  // phases that were still open.
   if (tid == 0 || pt == 0) umma::commit(&ms.bar_exit);   // arrives once this thread's MMAs are done
   umma::mbar_wait_bounded(&ms.bar_exit, 0, kWaitLimit);
+  if (!is_chain && *(volatile int *)&ms.err != 0) {
+    // a copy issued for a chunk that was never processed may still be landing: wait for the
+    // next phase of each copy barrier (returns at once if it completes, gives up otherwise)
+    umma::mbar_wait_bounded(&ms.bar_in, in_done & 1u, kWaitLimit);
+    if (pt == 0) umma::mbar_wait_bounded(&ms.bar_m, m_done & 1u, kWaitLimit);
+  }
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
@@ -474,20 +504,20 @@ recur_tc_kernel(const Problem p) {
 }
 
 template <int K>
-static cudaError_t launch_recur_t(const Problem &p, cudaStream_t stream) {
+static cudaError_t launch_recur_t(const Problem &p, const TmaMaps &maps, cudaStream_t stream) {
   const size_t smem = RecLayout<K>::bytes;
   static_assert(sizeof(RecMisc<K>) <= 4096, "misc block");
   cudaError_t e = cudaFuncSetAttribute(recur_tc_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)p.N * p.H * (p.V / kBV);
-  recur_tc_kernel<K><<<(unsigned)grid, kRecThreads, smem, stream>>>(p);
+  recur_tc_kernel<K><<<(unsigned)grid, kRecThreads, smem, stream>>>(p, maps);
   return cudaGetLastError();
 }
 
-cudaError_t launch_recur(const Problem &p, cudaStream_t stream) {
+cudaError_t launch_recur(const Problem &p, const TmaMaps &maps, cudaStream_t stream) {
   if (p.N == 0) return cudaSuccess;
-  return p.K == 64 ? launch_recur_t<64>(p, stream) : launch_recur_t<128>(p, stream);
+  return p.K == 64 ? launch_recur_t<64>(p, maps, stream) : launch_recur_t<128>(p, maps, stream);
 }
 
 }  // namespace kda

@@ -150,7 +150,7 @@ def fwd_noalloc(q, k, v, g, beta, A_log, dt_bias=None, lower_bound=-5.0, scale=N
 
 
 def debug_chunk_matrices(q, k, g, beta, A_log, dt_bias=None, lower_bound=-5.0, cu_seqlens=None):
-    """The prep kernel's per-(chunk, head) hand-off matrices, fp16 [max_chunks, H, 128, 64]."""
+    """The prep kernel's per-(chunk, head) hand-off matrices, fp16 [max_chunks, H, 128, 64] (row-major)."""
     B, T, H, K = q.shape
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
     mc = max_chunks(B, T, N)
@@ -161,7 +161,12 @@ def debug_chunk_matrices(q, k, g, beta, A_log, dt_bias=None, lower_bound=-5.0, c
                                             _ptr(dt_bias), float(lower_bound), _ptr(cu_seqlens), B, T,
                                             H, K, N, _ptr(mats), _ptr(ws), ws.numel(), _stream_ptr())
     check("kda_debug_chunk_matrices", rc)
-    return mats[:mc]
+    # undo the 128-byte swizzle of the stored blocks: chunk c of row r sits at r*8 + (c ^ (r % 8))
+    r = torch.arange(128, device=mats.device).view(128, 1)
+    c = torch.arange(8, device=mats.device).view(1, 8)
+    src = (c ^ (r % 8)).view(1, 1, 128, 8, 1).expand(mats.shape[0], H, 128, 8, 8)
+    blocks = mats[:mc].view(mc, H, 128, 8, 8)
+    return torch.gather(blocks, 3, src[:mc]).view(mc, H, 128, 64)
 
 
 def device_status(stream=None) -> int:

@@ -154,12 +154,15 @@ KDA_API kda_status_t kda_fwd_with_events(const void *q, const void *k, const voi
  * prep kernel of kda_fwd() and copies, for every chunk c (in sequence order,
  * chunk c of sequence s at index chunk_offset[s] + c, where chunk_offset is the
  * exclusive prefix sum of ceil(len_s / 64)) and head h, the fp16 matrix
- *   M[c,h] = [ -Tb ; P Tb ]  (128 x 64, row-major),  Tb = (I + A)^{-1} diag(beta)
+ *   M[c,h] = [ -Tb ; P Tb ]  (128 x 64),  Tb = (I + A)^{-1} diag(beta)
  * into `chunk_mats` (device, fp16 [max_chunks][H][128][64], max_chunks =
  * kda_max_chunks(B, T, num_seqs)). A, P are the decay-weighted strictly lower
  * key-key and lower query-key chunk matrices. Rows and columns past the end
- * of a partial chunk are zero (their beta is taken as 0). Same arguments and
- * errors as kda_fwd() otherwise.
+ * of a partial chunk are zero (their beta is taken as 0). Each 128 x 64 block
+ * is stored in the 128-byte-swizzled order the recurrence kernel loads it in:
+ * the 16-byte chunk c (8 values, columns 8c..8c+7) of row r sits at position
+ * r * 8 + (c XOR (r mod 8)) of the block. Same arguments and errors as
+ * kda_fwd() otherwise.
  */
 KDA_API kda_status_t kda_debug_chunk_matrices(const void *q, const void *k, const void *g,
                                       const void *beta, const float *A_log,
@@ -186,7 +189,7 @@ KDA_API kda_status_t kda_debug_chunk_matrices(const void *q, const void *k, cons
  *
  * Limit: the problem must fit in KDA_NOALLOC_MAX_SCRATCH bytes of scratch,
  * i.e. kda_fwd_workspace_size(B, T, H, K, V, num_seqs) <= KDA_NOALLOC_MAX_SCRATCH
- * (for example 16 MiB holds about 1000 (chunk, head) pairs: B=1, T=8192, H=7).
+ * (about 4 MiB per head per 8192 tokens at K = V = 128: B=1, T=8192 fits H <= 3).
  * Larger problems are rejected with KDA_ERR_WORKSPACE before anything runs.
  * Every GPU that loads the library holds this array until the process exits.
  *
