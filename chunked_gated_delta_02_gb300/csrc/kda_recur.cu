@@ -85,8 +85,9 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   using Lay = RecLayout<K>;
   constexpr int CPT = K / 64;   // channels per prep thread
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                        ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base, derived from the __shared__ array by pointer arithmetic so that the
+  // compiler keeps every access in the shared address space
+  unsigned char *sm = smem_raw + ((1024u - (umma::smem_u32(smem_raw) & 1023u)) & 1023u);
   __half *qt = reinterpret_cast<__half *>(sm + Lay::qt);
   __nv_bfloat16 *rq = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::rq);
   __nv_bfloat16 *rk = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::rk);
