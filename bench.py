@@ -62,13 +62,52 @@ def dist_env():
     return ws, rank, local
 
 
-def algorithmic_bytes(inp) -> int:
-    """Bytes the operation must move: read q,k,g,v,beta (+ initial state), write o (+ final state)."""
+def algorithmic_bytes(inp, with_state=True) -> int:
+    """Bytes the operation must move: read q,k,g,v,beta (+ initial state), write o (+ final state).
+
+    Per token-head that is 3K + V bf16 values and one bf16 beta in, V bf16 values out (1282 B at
+    K = V = 128); the state adds V K fp32 values per (sequence, head) for each direction used."""
     B, T, H, K, V, N = (inp[x] for x in ("B", "T", "H", "K", "V", "N"))
     th = B * T * H
     io = th * (3 * K * 2 + V * 2 + 2 + V * 2)
+    if not with_state:
+        return io
     state = N * H * V * K * 4
     return io + state * (1 if inp["initial_state"] is not None else 0) + state  # final_state written
+
+
+def max_over_ranks(vals, device=None):
+    """Element-wise maximum of a list of floats over all ranks (the list itself with one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(x) for x in vals]
+    t = torch.tensor([float(x) for x in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_rate(units_per_rank, world_size, ms_max):
+    """Units per second of the whole job: every rank processes its own replica of the workload, and
+    the job takes as long as its slowest rank."""
+    return units_per_rank * world_size / (ms_max * 1e-3)
+
+
+def kernel_rooflines(inp, ms_prep, ms_rec, peak, peak_src, workload):
+    """HBM roofline of each kernel: the algorithmic bytes of the launch over its measured time.
+
+    The prep kernel is credited with the token bytes (1282 B per token-head at K = V = 128), the
+    recurrence kernel with the token bytes plus the state. The dominant kernel (longer time) comes
+    first."""
+    out = []
+    for name, key, ms, ab in (("prep (K1)", "prep", ms_prep, algorithmic_bytes(inp, with_state=False)),
+                              ("recurrence (K2)", "recurrence", ms_rec, algorithmic_bytes(inp))):
+        gbs = ab / (ms * 1e-3) / 1e9
+        out.append({"bound": "hbm", "kernel": name, "achieved": gbs, "peak": peak, "unit": "GB/s",
+                    "frac": gbs / peak, "traffic": ncu_traffic(workload, key),
+                    "algorithmic_bytes_per_launch": ab, "ms_per_launch": ms, "peak_source": peak_src})
+    out.sort(key=lambda r: -r["ms_per_launch"])
+    return out
 
 
 def tokens_of(inp) -> int:
@@ -299,27 +338,21 @@ def run_ours(args):
     ms = statistics.mean(tot)
     ms_rec = statistics.mean(rec)
     ms_prep = statistics.mean(prep)
-    if ws > 1:
-        t = torch.tensor([ms, ms_rec, ms_prep], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, ms_rec, ms_prep = (float(x) for x in t.tolist())
+    ms, ms_rec, ms_prep = max_over_ranks([ms, ms_rec, ms_prep], dev)
     e2e = None if args.no_e2e else run_e2e(args, inp, dev, kda, o, fs, wsb)
     if rank == 0:
         peak, peak_src = measured_peak()
         abytes = algorithmic_bytes(inp)
-        achieved = abytes / (ms_rec * 1e-3) / 1e9
         path_gbs = abytes / (ms * 1e-3) / 1e9
+        roofs = kernel_rooflines(inp, ms_prep, ms_rec, peak, peak_src, args.workload)
         kernels_per_step = 2 + (1 if inp["cu_seqlens"] is not None else 0)
-        out = {"metric": METRIC, "value": tokens_of(inp) * ws / (ms * 1e-3), "unit": UNIT, "impl": "ours",
+        out = {"metric": METRIC, "value": whole_job_rate(tokens_of(inp), ws, ms), "unit": UNIT, "impl": "ours",
                "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                "data": "synthetic", "config": workload_desc(args.workload, inp),
-               "roofline": {"bound": "hbm", "kernel": "recurrence (K2)", "achieved": achieved, "peak": peak,
-                            "unit": "GB/s", "frac": achieved / peak,
-                            "traffic": ncu_traffic(args.workload, "recurrence"),
-                            "algorithmic_bytes_per_launch": abytes, "ms_per_launch": ms_rec,
-                            "peak_source": peak_src},
-               "path_roofline": {"achieved": path_gbs, "frac": path_gbs / peak,
+               "roofline": roofs[0], "roofline_other_kernel": roofs[1],
+               "path_roofline": {"achieved": path_gbs, "frac": path_gbs / peak, "unit": "GB/s",
+                                 "algorithmic_bytes_per_step": abytes,
                                  "ms_prep": ms_prep, "ms_recurrence": ms_rec},
                "gpu_launches": kernels_per_step * args.steps,
                "wall_s_timed_region": wall, "clocks": clk}

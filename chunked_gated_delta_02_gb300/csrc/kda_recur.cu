@@ -24,7 +24,7 @@
 // Warp roles (the S-independent work of chunk n+1 overlaps the state chain of
 // chunk n):
 //   chain group, warps 0-3: D2 += WQ S, U and o, D3 = k~^T U, S update.
-//   prep group, warps 4-11: stages the chunk inputs with cp.async, computes
+//   prep group, warps 4-11: stages the chunk inputs with TMA, computes
 //     the gate, the decay products and the fp16 operands (one thread per
 //     channel pair and 16-row block), issues D1 and D2, and forms WQ and k~.
 // The groups hand over through mbarriers. Every wait gives up after a bounded

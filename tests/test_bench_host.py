@@ -1,0 +1,77 @@
+"""Host logic of bench.py for more than one rank, on CPU with the gloo backend.
+
+The path has no exchange step: each rank runs its own replica of the workload,
+the timing is the maximum over ranks, and the whole-job rate counts every
+rank's tokens. These tests run that logic as two real processes.
+"""
+from __future__ import annotations
+
+import io
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, results):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ws, r, local = bench.dist_env()
+        # rank r took (r + 1) ms for the whole step and (10 - r) ms for one stage
+        mx = bench.max_over_ranks([rank + 1.0, 10.0 - rank])
+        rate = bench.whole_job_rate(4096, ws, mx[0])
+        # the reference arm: only rank 0 runs and prints
+        args = type("A", (), {"workload": "tiny", "seed": 0, "steps": 0, "warmup": 0})()
+        buf = io.StringIO()
+        if rank != 0:
+            with redirect_stdout(buf):
+                bench.run_reference(args)
+        results[rank] = (ws, r, local, mx, rate, buf.getvalue())
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_max_and_whole_job_rate():
+    world = 2
+    with mp.Manager() as m:
+        results = m.dict()
+        mp.spawn(_worker, args=(world, _free_port(), results), nprocs=world, join=True)
+        res = dict(results)
+    assert sorted(res) == [0, 1]
+    for rank, (ws, r, local, mx, rate, printed) in res.items():
+        assert (ws, r, local) == (2, rank, rank)
+        assert mx == [2.0, 10.0]                      # maximum over both ranks, element by element
+        assert rate == pytest.approx(2 * 4096 / 2e-3)  # both ranks' tokens over the slowest rank's time
+    assert res[1][5] == ""                            # rank 1 of the reference arm prints nothing
+
+
+def test_single_process_helpers():
+    assert bench.max_over_ranks([1.5, 2]) == [1.5, 2.0]
+    assert bench.whole_job_rate(1000, 1, 2.0) == pytest.approx(5e5)
+
+
+def test_algorithmic_bytes_fixed_workload():
+    from chunked_gated_delta_02_gb300.workloads import named
+    w = named("fixed")
+    inp = {"B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V, "N": w.B, "initial_state": None}
+    th = 2 * 2048 * 32
+    assert bench.algorithmic_bytes(inp, with_state=False) == th * 1282
+    assert bench.algorithmic_bytes(inp) == th * 1282 + 2 * 32 * 128 * 128 * 4
