@@ -1,10 +1,11 @@
 // K1: token-parallel prep kernel of the KDA chunked forward.
 //
-// One CTA per (chunk of 64 tokens, head). It does the work of the FlashKDA
-// "K1" stage (FlashKDA page, section "커널 퓨전(Kernel Fusion) 전략의 분리":
-// gate activation, L2 normalisation, decay, and the triangular inverse, all
-// parallel over tokens) and the cuLA "kda chunk intra" stage (cuLA launch
-// blog, section "Status & Roadmap"), and hands the recurrence kernel:
+// One CTA per (chunk of 64 tokens, head), two CTAs per SM. It does the work of
+// the FlashKDA "K1" stage (FlashKDA page, section "커널 퓨전(Kernel Fusion)
+// 전략의 분리": gate activation, L2 normalisation, decay and the triangular
+// inverse, all parallel over tokens) and the cuLA "kda chunk intra" stage
+// (cuLA launch blog, section "Status & Roadmap"), and hands the recurrence
+// kernel:
 //   * the per-token base-2 log decay la2 = lb log2(e) sigmoid(exp(A_log)(g + dt_bias)),
 //     rounded to fp16 (both kernels use the rounded value);
 //   * one 128 x 64 fp16 matrix per (chunk, head), stored in the 128-byte-swizzled
@@ -17,82 +18,96 @@
 // with G the in-chunk cumulative base-2 log decay. With M the recurrence kernel
 // forms w = Tb (khat 2^G), u = Tb v, P w and P u as plain products.
 //
+// Norms. khat = k / |k| and qhat = q / |q| are per-row scalings, so they are
+// taken out of the sums: the products run on the raw bf16 values and the read
+// back scales entry (i, j) by beta_i |k_i|^-1 |k_j|^-1 (A) or |q_i|^-1 |k_j|^-1 (P).
+//
 // Exponent range. With lower_bound >= -5 one token decays by at most e^-5, so
 // over 16 tokens |G| <= 80 ln-units (about 115.4 in base 2), which fits in
 // fp32. Each 16-row block J keeps its own reference (the decay before the
-// block): X_i = 2^{Gb_i} <= 1 and Y_j = 2^{-Gb_j} >= 1 with Gb the block-local
-// cumulative sum. For j in block J < i in block I,
-//   2^{G_i - G_j} = [X_i] [Y_j 2^{B_J} c_IJ],
-// where B_J is the whole-block sum of block J and c_IJ = 2^{sum of the blocks
-// strictly between J and I}: the J-side factor Y_j 2^{B_J} is <= 1 and so is
-// c_IJ, so nothing overflows and a factor only underflows when the true
-// product is already below the fp32 range. Diagonal blocks use X_i Y_j
-// directly (<= 2^115.4). This is the "intra-chunk rescaling" that large
-// chunks need (FlashKDA page, section "Flash Linear Attention과 비교").
+// block). With alpha = 2^{la2} per token and channel:
+//   X_i  = prod of alpha over the block's rows up to and including i   (<= 1)
+//   Ys_j = prod of alpha over the block's rows after j                 (<= 1)
+//   Y_j  = 2^{-Gb_j} = Ys_j 2^{-B_J}                                   (>= 1)
+// with Gb the block-local inclusive cumulative sum and B_J the whole-block sum.
+// For j in block J < i in block I,  2^{G_i - G_j} = X_i Ys_j c_IJ, where
+// c_IJ = 2^{sum of the blocks strictly between J and I} <= 1: no factor
+// overflows, and one only underflows when the true product is already below the
+// fp32 range. Diagonal blocks use X_i Y_j (<= 2^115.4). This is the
+// "intra-chunk rescaling" that large chunks need (FlashKDA page, section
+// "Flash Linear Attention과 비교").
 //
 // All block products of A and P come from ONE tensor-core product (tcgen05,
-// tf32 operands, fp32 accumulators in tensor memory):
-//   D = [khat X ; qhat X] (128 x K)  x  [khat Y ; Ys ; Ys_0 2^{B_1} ; Ys_1 2^{B_2} ; Ys_0 c_30]^T
-// with Ys = khat Y 2^{B_J}: columns 0-63 give the diagonal blocks, 64-127 the
-// blocks next to the diagonal, 128-175 the three blocks further out.
-// The unit lower triangular inverse T = (I + A)^{-1} is blocked: the four
-// 16 x 16 diagonal blocks by right-looking forward substitution (one thread
-// per column, the column in registers), then the off-diagonal blocks level by
-// level, T_IJ = -T_II sum_{J<=M<I} A_IM T_MJ, in fp32. Finally M = [-I ; P] Tb
-// is a second tensor-core product (128 x 64 x 64).
+// tf32 operands, fp32 accumulators in tensor memory), accumulated over two
+// halves of the channels so that the operands fit twice per SM:
+//   D = [k X ; q X] (128 x K)  x  [k Y ; k Ys ; k Ys_0 2^{B_1} ; k Ys_1 2^{B_2} ; k Ys_0 c_30]^T
+// Columns 0-63 give the diagonal blocks, 64-127 the blocks next to the
+// diagonal, 128-175 the three blocks further out. The unit lower triangular
+// inverse T = (I + A)^{-1} is blocked: the four 16 x 16 diagonal blocks by
+// forward substitution (one thread per column), then the off-diagonal blocks
+// level by level, T_IJ = -T_II sum_{J<=M<I} A_IM T_MJ, in fp32. Finally
+// M = [-I ; P] Tb is a second tensor-core product (128 x 64 x 64).
 #include "kda_common.cuh"
 #include "umma.cuh"
 
 namespace kda {
 
-constexpr int kPrepThreads = 512;
+constexpr int kPrepThreads = 256;
 constexpr int kOpBRows = 176;                 // J-side operand rows
 constexpr uint32_t kPrepTmemCols = 256;       // D_AP: cols 0..175; D_M: cols 192..255
 constexpr long long kPrepWaitLimit = 4000000000LL;
 
-template <int K>
+// Shared memory (byte offsets from the 1024-aligned base). The operands hold one half of the
+// channels (64) at a time, as tf32 in 128-byte-swizzled panels of 32 channels.
 struct PrepLayout {
-  static constexpr uint32_t NP = K / 32;                    // tf32 panels along K
-  static constexpr uint32_t raw = 0;                        // bf16 q, k, g [64][K]
-  static constexpr uint32_t opA = 3 * 64 * K * 2;           // [khat X ; qhat X]: NP x 128 rows x 128 B
-  static constexpr uint32_t opB = opA + NP * 128 * 128;     // J side: NP x 176 rows x 128 B
-  static constexpr uint32_t end = opB + NP * kOpBRows * 128;
-  // after the A/P product the raw inputs and the I-side operand are dead: A and T (fp32
-  // [64][68]), the merge scratch and the Tb^T operand reuse them; the [-I ; P] operand
-  // reuses the J-side operand
-  static constexpr int LD = 68;                             // 68 = 4 (mod 32) words: conflict-free rows
+  static constexpr uint32_t opA = 0;                            // [k X ; q X]: 2 panels x 128 rows x 128 B
+  static constexpr uint32_t opB = opA + 2 * 128 * 128;          // J side:      2 panels x 176 rows x 128 B
+  static constexpr uint32_t opEnd = opB + 2 * kOpBRows * 128;
+  // after the A/P product the operands are dead: A and T (fp32 [64][68]), the merge scratch,
+  // the Tb^T operand and the [-I ; P] operand take their place
+  static constexpr int LD = 68;                                 // 68 = 4 (mod 32) words: conflict-free rows
   static constexpr uint32_t matA = 0;
   static constexpr uint32_t matT = matA + 64 * LD * 4;
-  static constexpr uint32_t Z = matT + 64 * LD * 4;         // [3][16][17] fp32
-  static constexpr uint32_t opT = 38 * 1024;                // Tb^T:     2 panels x  64 rows x 128 B
-  static constexpr uint32_t opM = opB;                      // [-I ; P]: 2 panels x 128 rows x 128 B
+  static constexpr uint32_t Z = matT + 64 * LD * 4;             // [3][16][17] fp32
+  static constexpr uint32_t opT = 38 * 1024;                    // Tb^T:     2 panels x  64 rows x 128 B
+  static constexpr uint32_t opM = 54 * 1024;                    // [-I ; P]: 2 panels x 128 rows x 128 B
+  static constexpr uint32_t end = opM + 2 * 128 * 128;
   static_assert(Z + 3 * 16 * 17 * 4 <= opT, "A/T/Z overlap the Tb^T operand");
-  static_assert(opT + 2 * 64 * 128 <= opB, "Tb^T operand overlaps the [-I ; P] operand");
-  static_assert(opM + 2 * 128 * 128 <= end, "[-I ; P] operand must fit in the J-side region");
+  static_assert(opT + 2 * 64 * 128 <= opM, "Tb^T operand overlaps the [-I ; P] operand");
+  static_assert(end >= opEnd, "layout end");
 };
 
 struct PrepMisc {
   uint64_t bar;
   uint32_t tmem_slot;
   int err;
-  float kn[kChunk], qn[kChunk], beta[kChunk];
+  float beta[kChunk], kn[kChunk], qn[kChunk];
+  float ksq[2][kChunk], qsq[2][kChunk];   // per half of the channels: row sums of squares
+  float2 ssub[4][2][32];                  // per (block, 8-row sub-block, channel pair): sum of la2
 };
 
+__device__ __forceinline__ uint32_t ldg_u32(const __nv_bfloat16 *p) {
+  return __ldg(reinterpret_cast<const unsigned int *>(p));
+}
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+__device__ __forceinline__ float2 ex2_2(float2 x) { return make_float2(ex2_approx(x.x), ex2_approx(x.y)); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+// two tf32-rounded values, stored as one 8-byte word
+__device__ __forceinline__ void st_tf32x2(unsigned char *p, float2 v) {
+  *reinterpret_cast<float2 *>(p) = make_float2(to_tf32(v.x), to_tf32(v.y));
+}
+
 template <int K>
-__global__ void __launch_bounds__(kPrepThreads, 1)
+__global__ void __launch_bounds__(kPrepThreads, 2)
 prep_kernel(const Problem p) {
-  using Lay = PrepLayout<K>;
+  using Lay = PrepLayout;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // 1024-byte aligned base, derived from the __shared__ array by pointer arithmetic so that the
   // compiler keeps every access in the shared address space
   unsigned char *sm = smem_raw + ((1024u - (umma::smem_u32(smem_raw) & 1023u)) & 1023u);
-  __nv_bfloat16 *rq = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::raw);
-  __nv_bfloat16 *rk = rq + 64 * K;
-  __nv_bfloat16 *rg = rk + 64 * K;
-  float *Bs = reinterpret_cast<float *>(sm + Lay::end);      // [4][K] whole-block log2 decay
-  float *eB = Bs + 4 * K;                                     // [4][K] 2^{B_J}
-  float *c12 = eB + 4 * K;                                    // [K]    (spare)
-  PrepMisc &ms = *reinterpret_cast<PrepMisc *>(c12 + K);
+  PrepMisc &ms = *reinterpret_cast<PrepMisc *>(sm + Lay::end);
   float (*matA)[Lay::LD] = reinterpret_cast<float (*)[Lay::LD]>(sm + Lay::matA);
   float (*matT)[Lay::LD] = reinterpret_cast<float (*)[Lay::LD]>(sm + Lay::matT);
   float (*Zs)[16][17] = reinterpret_cast<float (*)[16][17]>(sm + Lay::Z);
@@ -110,141 +125,183 @@ prep_kernel(const Problem p) {
   const int len = min(kChunk, si.len - n * kChunk);
   const uint32_t sbase = umma::smem_u32(sm);
 
-  // ---- pass 0: stage q, k, g rows (zero-filled past the chunk end); beta sigmoid; TMEM, barrier
-  stage_rows_async<K, kPrepThreads>(rq, p.q, p, si.b, t0, h, len, 0, K, tid);
-  stage_rows_async<K, kPrepThreads>(rk, p.k, p, si.b, t0, h, len, 0, K, tid);
-  stage_rows_async<K, kPrepThreads>(rg, p.g, p, si.b, t0, h, len, 0, K, tid);
-  cp_async_commit();
+  // ---- pass 0: beta sigmoid, TMEM, barrier
   if (tid < kChunk)
     ms.beta[tid] = (tid < len) ? sigmoid_fast(__bfloat162float(p.beta[tok_row(p, si.b, t0 + tid, h)])) : 0.f;
   if (warp == 0) {
     umma::tmem_alloc(&ms.tmem_slot, kPrepTmemCols);
     umma::tmem_relinquish();
   }
-  if (tid == 0) {
+  if (tid == 32) {
     umma::mbar_init(&ms.bar, 1);
     umma::mbar_fence_init();
     ms.err = 0;
   }
-  cp_async_wait_all();
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
   const uint32_t tmem = ms.tmem_slot;
-
-  // ---- pass 1: row norms (one warp per row, lanes across channels)
-#pragma unroll 1
-  for (int i = warp; i < kChunk; i += kPrepThreads / 32) {
-    float ssk = 0.f, ssq = 0.f;
-    const __nv_bfloat162 *kr = reinterpret_cast<const __nv_bfloat162 *>(rk + i * K);
-    const __nv_bfloat162 *qr = reinterpret_cast<const __nv_bfloat162 *>(rq + i * K);
-#pragma unroll
-    for (int x = lane; x < K / 2; x += 32) {
-      const float2 a = __bfloat1622float2(kr[x]), b = __bfloat1622float2(qr[x]);
-      ssk += a.x * a.x + a.y * a.y;
-      ssq += b.x * b.x + b.y * b.y;
-    }
-    ssk = warp_sum(ssk);
-    ssq = warp_sum(ssq);
-    if (lane == 0) {
-      ms.kn[i] = (i < len) ? rsqrtf(ssk + kNormEps) : 0.f;
-      ms.qn[i] = (i < len) ? rsqrtf(ssq + kNormEps) : 0.f;
-    }
-  }
-  __syncthreads();
-
-  // ---- pass 2: per (channel, 16-row block): gate and block-local decay, operands of the A/P product.
-  // The loops over the 16 rows are kept rolled: the kernel runs once per CTA, so its speed is set
-  // by instruction fetch as much as by issue, and short loop bodies keep the code small.
-  auto opA_at = [&](int row, int kc) -> float * {
-    return reinterpret_cast<float *>(sm + Lay::opA + (uint32_t)(kc >> 5) * (128 * 128) +
-                                     umma::sw128_offset32(row, kc & 31));
-  };
-  auto opB_at = [&](int row, int kc) -> float * {
-    return reinterpret_cast<float *>(sm + Lay::opB + (uint32_t)(kc >> 5) * (kOpBRows * 128) +
-                                     umma::sw128_offset32(row, kc & 31));
-  };
-  const bool unit_on = tid < 4 * K;
-  const int kk = tid % K, J = tid / K;   // unit = (channel kk, block J) when unit_on
-  // the fp16 log decay of (row, kk) replaces g in place: only this unit reads either
-  __half *rla = reinterpret_cast<__half *>(rg);
-  if (unit_on) {
-    const float ea = expf(p.A_log[h]);
-    const float lbl2 = p.lb * kLog2e;
-    const float dt = p.dt_bias ? p.dt_bias[h * K + kk] : 0.f;
-    const long long gstride = (long long)p.H * K;
-    __half *la_out = p.la2 + tok_row(p, si.b, t0 + 16 * J, h) * K + kk;
-    float Bsum = 0.f;
-#pragma unroll 1
-    for (int r = 0; r < 16; ++r) {
-      const int i = 16 * J + r;
-      __half la = __float2half_rn(0.f);
-      if (i < len) {
-        // rounded to fp16 once; this kernel and the recurrence kernel both use the rounded value
-        la = __float2half_rn(log2_decay(__bfloat162float(rg[i * K + kk]), dt, ea, lbl2));
-        la_out[r * gstride] = la;
-      }
-      rla[i * K + kk] = la;
-      Bsum += __half2float(la);
-    }
-    Bs[J * K + kk] = Bsum;
-  }
-  __syncthreads();
-  if (unit_on) {
-    // row i of block J (Gb = block-local inclusive cumulative decay):
-    //   I side   kX, qX with X = 2^{Gb}
-    //   J side   kY (row i), Ys = k 2^{B_J - Gb} (row 64 + i), and for the blocks two and three
-    //            away from the diagonal Ys 2^{B_1} (J = 0, row 128 + r), Ys 2^{B_2} (J = 1,
-    //            row 144 + r) and Ys 2^{B_1 + B_2} (J = 0, row 160 + r); every exponent is <= 0
-    const float BJ = Bs[J * K + kk], B1 = Bs[K + kk], B2 = Bs[2 * K + kk];
-    const int xrow = (J == 0) ? 128 : 144;
-    const float xe = (J == 0) ? B1 : B2;
-    float Gb = 0.f;
-#pragma unroll 1
-    for (int r = 0; r < 16; ++r) {
-      const int i = 16 * J + r;
-      Gb += __half2float(rla[i * K + kk]);
-      const float kv = __bfloat162float(rk[i * K + kk]) * ms.kn[i];
-      const float qv = __bfloat162float(rq[i * K + kk]) * ms.qn[i];
-      const float X = ex2_approx(Gb), e = BJ - Gb;
-      *opA_at(i, kk) = to_tf32(kv * X);      // operands rounded to nearest tf32
-      *opA_at(64 + i, kk) = to_tf32(qv * X);
-      *opB_at(i, kk) = to_tf32(kv * ex2_approx(-Gb));
-      *opB_at(64 + i, kk) = to_tf32(kv * ex2_approx(e));
-      if (J < 2) *opB_at(xrow + r, kk) = to_tf32(kv * ex2_approx(e + xe));
-      if (J == 0) *opB_at(160 + r, kk) = to_tf32(kv * ex2_approx(e + B1 + B2));
-    }
-  }
-  umma::fence_proxy_async_smem();
-  umma::fence_before_sync();
-  __syncthreads();
-
-  // ---- pass 3: all A and P blocks in one tcgen05 product (tf32), accumulator in TMEM cols 0..175
-  if (tid == 0) {
+  uint32_t waits = 0;   // completed waits on ms.bar (its phase parity)
+  auto wait_mma = [&]() {
+    if (!umma::mbar_wait_bounded(&ms.bar, waits & 1, kPrepWaitLimit)) atomicExch(&ms.err, 1);
+    ++waits;
     umma::fence_after_sync();
-    const uint32_t id = umma::idesc_tf32(128, kOpBRows, 0, 0);
+  };
+
+  // Elementwise unit of this thread: channel pair `lane` of the current half, 16-row block
+  // J = warp / 2, 8-row sub-block sb = warp % 2.
+  const int J = warp >> 1, sb = warp & 1;
+  const int row0 = 16 * J + 8 * sb;
+  const int nrows = max(0, min(8, len - row0));
+  const float ea = expf(p.A_log[h]);
+  const float cg = -ea * kLog2e;                 // sigmoid(a) = 1 / (1 + 2^{cg (g + dt)})
+  const float lbl2 = p.lb * kLog2e;
+  const long long rstride = (long long)p.H * K;  // elements between consecutive tokens
+  const long long rbase = tok_row(p, si.b, t0 + row0, h) * K;
+  // swizzled byte offset of this lane's channel pair inside a row (row & 7 == r for row0 + r)
+  const uint32_t pan = (uint32_t)(lane >> 4), chk = (uint32_t)((lane & 15) >> 1), sub8 = (uint32_t)(lane & 1) * 8;
+  auto op_at = [&](uint32_t region, uint32_t rows_per_panel, int row, int r) -> unsigned char * {
+    return sm + region + pan * (rows_per_panel * 128) + (uint32_t)row * 128 + (((chk ^ (uint32_t)r) << 4) | sub8);
+  };
+
 #pragma unroll 1
-    for (int ks = 0; ks < K / 8; ++ks) {
-      const uint64_t a = umma::sdesc_sw128(sbase + Lay::opA + (ks >> 2) * (128 * 128) + (ks & 3) * 32, 16, 1024);
-      const uint64_t b =
-          umma::sdesc_sw128(sbase + Lay::opB + (ks >> 2) * (kOpBRows * 128) + (ks & 3) * 32, 16, 1024);
-      umma::mma_tf32_ss(tmem, a, b, id, ks > 0);
+  for (int hf = 0; hf < K / 64; ++hf) {
+    // ---- pass 1: gate, log decay to fp16, raw q and k of 8 rows x 2 channels, row norms
+    const int kk = 64 * hf + 2 * lane;
+    uint32_t rawk[8], rawq[8], rawg[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      rawk[r] = rawq[r] = rawg[r] = 0u;
+      if (r < nrows) {
+        const long long off = rbase + r * rstride + kk;
+        rawg[r] = ldg_u32(p.g + off);
+        rawk[r] = ldg_u32(p.k + off);
+        rawq[r] = ldg_u32(p.q + off);
+      }
     }
-    umma::commit(&ms.bar);
+    float2 dt = make_float2(0.f, 0.f);
+    if (p.dt_bias) dt = *reinterpret_cast<const float2 *>(p.dt_bias + h * K + kk);
+    const float2 cdt = make_float2(cg * dt.x, cg * dt.y);
+    float2 al[8], kv[8], qv[8];
+    float2 ssum = make_float2(0.f, 0.f);
+    float red[16];   // per row: |k|^2 and |q|^2 over this lane's two channels
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const float2 g2 = bf2_to_f2(rawg[r]);
+      const float2 e = __ffma2_rn(make_float2(cg, cg), g2, cdt);
+      const float2 sg = make_float2(rcp_approx(1.f + ex2_approx(e.x)), rcp_approx(1.f + ex2_approx(e.y)));
+      // rounded to fp16 once; this kernel and the recurrence kernel both use the rounded value
+      __half2 la = __floats2half2_rn(lbl2 * sg.x, lbl2 * sg.y);
+      if (r < nrows)
+        *reinterpret_cast<__half2 *>(p.la2 + rbase + r * rstride + kk) = la;
+      else
+        la = __floats2half2_rn(0.f, 0.f);
+      const float2 laf = __half22float2(la);
+      ssum.x += laf.x;
+      ssum.y += laf.y;
+      al[r] = ex2_2(laf);
+      kv[r] = bf2_to_f2(rawk[r]);
+      qv[r] = bf2_to_f2(rawq[r]);
+      red[r] = kv[r].x * kv[r].x + kv[r].y * kv[r].y;
+      red[8 + r] = qv[r].x * qv[r].x + qv[r].y * qv[r].y;
+    }
+    ms.ssub[J][sb][lane] = ssum;
+    // reduce-scatter of the 16 row sums over the warp: after the five steps lane l holds the
+    // full sum of value v(l) = 8 b4 + 4 b3 + 2 b2 + b1 (b = bits of l)
+#pragma unroll
+    for (int w = 8, bit = 16; w >= 1; w >>= 1, bit >>= 1) {
+      const bool up = (lane & bit) != 0;
+#pragma unroll
+      for (int j = 0; j < w; ++j) {
+        const float send = up ? red[j] : red[j + w];
+        const float keep = up ? red[j + w] : red[j];
+        red[j] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+      }
+    }
+    red[0] += __shfl_xor_sync(0xffffffffu, red[0], 1);
+    if ((lane & 1) == 0) {
+      const int v = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+      if (v < 8) ms.ksq[hf][row0 + v] = red[0];
+      else ms.qsq[hf][row0 + v - 8] = red[0];
+    }
+    __syncthreads();
+
+    // ---- pass 2: operands of the A/P product for this half (tf32, rounded to nearest)
+    const float2 S0 = ms.ssub[J][0][lane], S1 = ms.ssub[J][1][lane];
+    const float2 BJ = make_float2(S0.x + S1.x, S0.y + S1.y);
+    float2 X = sb ? ex2_2(S0) : make_float2(1.f, 1.f);     // decay from the block start to row0 - 1
+    float2 suf = sb ? make_float2(1.f, 1.f) : ex2_2(S1);   // decay over the block rows after the sub-block
+    const float2 eBinv = ex2_2(make_float2(-BJ.x, -BJ.y));
+    float2 x1 = make_float2(0.f, 0.f), x2 = make_float2(0.f, 0.f);
+    if (J == 0) {
+      const float2 a = ms.ssub[1][0][lane], b = ms.ssub[1][1][lane];
+      const float2 c2 = ms.ssub[2][0][lane], d = ms.ssub[2][1][lane];
+      const float2 B1 = make_float2(a.x + b.x, a.y + b.y), B2 = make_float2(c2.x + d.x, c2.y + d.y);
+      x1 = ex2_2(B1);
+      x2 = ex2_2(make_float2(B1.x + B2.x, B1.y + B2.y));
+    } else if (J == 1) {
+      const float2 c2 = ms.ssub[2][0][lane], d = ms.ssub[2][1][lane];
+      x1 = ex2_2(make_float2(c2.x + d.x, c2.y + d.y));
+    }
+    const int xrow = (J == 0) ? 128 : 144;
+    if (hf > 0) wait_mma();   // the previous half's product has read the operands
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {   // I side
+      X = mul2(X, al[r]);
+      st_tf32x2(op_at(Lay::opA, 128, row0 + r, r), mul2(kv[r], X));
+      st_tf32x2(op_at(Lay::opA, 128, 64 + row0 + r, r), mul2(qv[r], X));
+    }
+#pragma unroll
+    for (int r = 7; r >= 0; --r) {  // J side
+      const float2 ys = mul2(kv[r], suf);
+      suf = mul2(suf, al[r]);
+      st_tf32x2(op_at(Lay::opB, kOpBRows, row0 + r, r), mul2(ys, eBinv));
+      st_tf32x2(op_at(Lay::opB, kOpBRows, 64 + row0 + r, r), ys);
+      if (J < 2) st_tf32x2(op_at(Lay::opB, kOpBRows, xrow + 8 * sb + r, r), mul2(ys, x1));
+      if (J == 0) st_tf32x2(op_at(Lay::opB, kOpBRows, 160 + 8 * sb + r, r), mul2(ys, x2));
+    }
+    umma::fence_proxy_async_smem();
+    umma::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      umma::fence_after_sync();
+      const uint32_t id = umma::idesc_tf32(128, kOpBRows, 0, 0);
+#pragma unroll 1
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t a = umma::sdesc_sw128(sbase + Lay::opA + (ks >> 2) * (128 * 128) + (ks & 3) * 32, 16, 1024);
+        const uint64_t b =
+            umma::sdesc_sw128(sbase + Lay::opB + (ks >> 2) * (kOpBRows * 128) + (ks & 3) * 32, 16, 1024);
+        umma::mma_tf32_ss(tmem, a, b, id, (hf > 0) || (ks > 0));
+      }
+      umma::commit(&ms.bar);
+    }
   }
-  if (!umma::mbar_wait_bounded(&ms.bar, 0, kPrepWaitLimit)) atomicExch(&ms.err, 1);
-  umma::fence_after_sync();
-  // readback: warp w reads TMEM lanes 32 (w % 4) .. + 31 (lane = D row) and the 16-column blocks
-  // cb = w / 4, w / 4 + 4, w / 4 + 8. A rows (< 64) go to fp32 matA (times beta, strictly lower),
-  // P rows to the [-I ; P] operand (tf32, lower with the diagonal).
+
+  // ---- pass 3: norms, then read A and P back from TMEM (cols 0..175)
+  if (tid < kChunk) {
+    float ks2 = 0.f, qs2 = 0.f;
+#pragma unroll
+    for (int hf = 0; hf < K / 64; ++hf) {
+      ks2 += ms.ksq[hf][tid];
+      qs2 += ms.qsq[hf][tid];
+    }
+    ms.kn[tid] = (tid < len) ? rsqrtf(ks2 + kNormEps) : 0.f;
+    ms.qn[tid] = (tid < len) ? rsqrtf(qs2 + kNormEps) : 0.f;
+  }
+  wait_mma();
+  __syncthreads();
+  // warp w reads TMEM lanes 32 (w % 4) .. + 31 (lane = D row) and the 16-column blocks
+  // cb = w / 4, w / 4 + 2, ... A rows (< 64) go to fp32 matA (times beta_i |k_i|^-1 |k_j|^-1,
+  // strictly lower), P rows to the [-I ; P] operand (times |q_i|^-1 |k_j|^-1, lower with the
+  // diagonal, tf32).
   {
     const int row = 32 * (warp & 3) + lane, I = (row & 63) >> 4;
     const bool isA = row < 64;
-    const float mul = isA ? ms.beta[row] : 1.f;
+    const float rowf = isA ? ms.beta[row] * ms.kn[row] : ms.qn[row - 64];
     const int thr = isA ? row : row - 63;   // column j is kept when j < thr
     const int xs = isA ? 0 : (row & 7);
 #pragma unroll 1
-    for (int cb = warp >> 2; cb < kOpBRows / 16; cb += 4) {
+    for (int cb = warp >> 2; cb < kOpBRows / 16; cb += 2) {
       float x[16];
       umma::tmem_ld16(tmem + ((uint32_t)(warp & 3) * 32 << 16) + cb * 16, x);
       umma::tmem_ld_wait();
@@ -260,11 +317,13 @@ prep_kernel(const Problem p) {
       const int c0 = isA ? 4 * Jb : 4 * (Jb & 1);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
+        const float4 knj = *reinterpret_cast<const float4 *>(&ms.kn[16 * Jb + 4 * q]);
+        const float kj[4] = {knj.x, knj.y, knj.z, knj.w};
         float4 v;
         float *pv = &v.x;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float y = (16 * Jb + 4 * q + e < thr) ? x[4 * q + e] * mul : 0.f;
+          const float y = (16 * Jb + 4 * q + e < thr) ? x[4 * q + e] * rowf * kj[e] : 0.f;
           pv[e] = isA ? y : to_tf32(y);
         }
         *reinterpret_cast<float4 *>(rowp + (((c0 + q) ^ xs) << 4)) = v;
@@ -302,7 +361,7 @@ prep_kernel(const Problem p) {
       matT[o + j][o + col] = head;
       const float *aj = &matA[o + j][o + j];
 #pragma unroll
-      for (int s = 1; s < 16; ++s) x[s - 1] = fmaf((j + s < 16) ? -aj[s * Lay::LD] : 0.f, head, x[s]);
+      for (int s2 = 1; s2 < 16; ++s2) x[s2 - 1] = fmaf((j + s2 < 16) ? -aj[s2 * Lay::LD] : 0.f, head, x[s2]);
     }
   }
   __syncthreads();
@@ -355,17 +414,18 @@ prep_kernel(const Problem p) {
     }
     umma::commit(&ms.bar);
   }
-  if (!umma::mbar_wait_bounded(&ms.bar, 1, kPrepWaitLimit)) atomicExch(&ms.err, 1);
-  umma::fence_after_sync();
+  wait_mma();
   // output: row r of M (TMEM lane r) -> fp16, written in the swizzled chunk order r*8 + (cc ^ (r & 7));
-  // warp w takes lanes 32 (w % 4) .. + 31 and columns 16 (w / 4) .. + 15
+  // warp w takes lanes 32 (w % 4) .. + 31 and columns 32 (w / 4) .. + 31
   {
-    const int r = 32 * (warp & 3) + lane, c0 = 16 * (warp >> 2);
+    const int r = 32 * (warp & 3) + lane;
     uint4 *dst = reinterpret_cast<uint4 *>(p.mats + ((long long)c * p.H + h) * (2 * kChunk * kChunk)) + r * 8;
-    float x[16];
-    umma::tmem_ld16(tmem + 192 + ((uint32_t)(warp & 3) * 32 << 16) + c0, x);
-    umma::tmem_ld_wait();
-    if (!ms.err) {
+#pragma unroll 1
+    for (int c0 = 32 * (warp >> 2); c0 < 32 * (warp >> 2) + 32; c0 += 16) {
+      float x[16];
+      umma::tmem_ld16(tmem + 192 + ((uint32_t)(warp & 3) * 32 << 16) + c0, x);
+      umma::tmem_ld_wait();
+      if (ms.err) continue;
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
         const int cc = (c0 >> 3) + hc;
@@ -384,8 +444,8 @@ prep_kernel(const Problem p) {
 
 template <int K>
 static cudaError_t launch_prep_t(const Problem &p, cudaStream_t stream) {
-  using Lay = PrepLayout<K>;
-  const size_t smem = Lay::end + (9 * K) * sizeof(float) + sizeof(PrepMisc) + 1024;
+  using Lay = PrepLayout;
+  const size_t smem = Lay::end + sizeof(PrepMisc) + 1024;
   cudaError_t e = cudaFuncSetAttribute(prep_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
