@@ -27,7 +27,7 @@ constexpr size_t kMatBytes = 2ull * kda::kChunk * kda::kChunk * sizeof(__half); 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t flag_off, chunk_off_off, order_off, mats_off, la2_off, total;
+  size_t flag_off, chunk_off_off, order_off, mats_off, kg_off, kt_off, qt_off, gam_off, total;
 };
 
 bool sizes_ok(int B, int T, int H, int K, int V, int N) {
@@ -47,10 +47,18 @@ Layout layout_of(int B, int T, int H, int K, int N) {
   off = align_up(off + sizeof(int32_t) * ((size_t)N + 1));
   L.order_off = off;
   off = align_up(off + sizeof(int32_t) * ((size_t)N + 1));
+  const size_t ch = (size_t)max_chunks_of(B, T, N) * (size_t)H;   // (chunk, head) slots
+  const size_t img = (size_t)kda::kChunk * (size_t)K * sizeof(__half);
   L.mats_off = off;
-  off = align_up(off + (size_t)max_chunks_of(B, T, N) * (size_t)H * kMatBytes);
-  L.la2_off = off;
-  off = align_up(off + (size_t)B * (size_t)T * (size_t)H * (size_t)K * sizeof(__half));
+  off = align_up(off + ch * kMatBytes);
+  L.kg_off = off;
+  off = align_up(off + ch * img);
+  L.kt_off = off;
+  off = align_up(off + ch * img);
+  L.qt_off = off;
+  off = align_up(off + ch * img);
+  L.gam_off = off;
+  off = align_up(off + ch * (size_t)K * sizeof(float));
   L.total = off;
   return L;
 }
@@ -106,7 +114,7 @@ kda_status_t check_common(const void *q, const void *k, const void *g, const voi
     return KDA_ERR_INVALID_ARG;
   }
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(g, 16) || !aligned(beta, 2) ||
-      !aligned(A_log, 4) || (dt_bias && !aligned(dt_bias, 4)))
+      !aligned(A_log, 4) || (dt_bias && !aligned(dt_bias, 8)))
     return KDA_ERR_INVALID_ARG;
   // element counts must fit the 64-bit index arithmetic of the kernels
   const double elems = (double)B * (double)T * (double)H * (double)K;
@@ -163,7 +171,10 @@ kda_status_t fill_problem(kda::Problem &p, const Layout &L, void *ws, const void
   p.chunk_off = reinterpret_cast<int32_t *>(base + L.chunk_off_off);
   p.order = reinterpret_cast<int32_t *>(base + L.order_off);
   p.mats = reinterpret_cast<__half *>(base + L.mats_off);
-  p.la2 = reinterpret_cast<__half *>(base + L.la2_off);
+  p.kgimg = reinterpret_cast<__half *>(base + L.kg_off);
+  p.ktimg = reinterpret_cast<__half *>(base + L.kt_off);
+  p.qtb = reinterpret_cast<__half *>(base + L.qt_off);
+  p.gam = reinterpret_cast<float *>(base + L.gam_off);
   if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p.dev_status), g_kda_device_status) != cudaSuccess) {
     cudaGetLastError();
     return KDA_ERR_CUDA;
@@ -255,11 +266,7 @@ kda_status_t kda_fwd_with_events(const void *q, const void *k, const void *v, co
   mark(events ? events->prep_done : nullptr);
   kda::TmaMaps maps;
   std::memset(&maps, 0, sizeof maps);
-  if (st == KDA_OK && T > 0 &&
-      !(encode_token_map(&maps.q, q, K, H, T, B, K) && encode_token_map(&maps.k, k, K, H, T, B, K) &&
-        encode_token_map(&maps.la2, p.la2, K, H, T, B, K, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) &&
-        encode_token_map(&maps.v, v, V, H, T, B, 64)))
-    st = KDA_ERR_CUDA;
+  if (st == KDA_OK && T > 0 && !encode_token_map(&maps.v, v, V, H, T, B, 64)) st = KDA_ERR_CUDA;
   if (st == KDA_OK) st = from_cuda(kda::launch_recur(p, maps, s));
   mark(events ? events->recur_done : nullptr);
   release_scratch(scr, s);

@@ -31,8 +31,13 @@ struct Problem {
   float *final_state;                // [N,H,V,K] or null
   const int32_t *cu;                 // [N+1] or null (fixed length)
   __nv_bfloat16 *o;                  // [B,T,H,V]
-  __half *mats;                      // [max_chunks][H][2C][C] fp16 hand-off
-  __half *la2;                       // [B,T,H,K] fp16 per-token base-2 log decay (prep -> recurrence)
+  // prep -> recurrence hand-off, per (chunk, head); the two images are stored in the
+  // 128-byte-swizzled layout of the recurrence kernel's shared-memory operands
+  __half *mats;                      // [max_chunks][H][2C][C] fp16: M = [-Tb ; P Tb]
+  __half *kgimg;                     // [max_chunks][H][C x K] fp16: khat Gamma, MN-major image
+  __half *ktimg;                     // [max_chunks][H][C x K] fp16: khat Gamma_last / Gamma, MN-major image
+  __half *qtb;                       // [max_chunks][H][C][K] fp16: qhat Gamma, row-major
+  float *gam;                        // [max_chunks][H][K] fp32: Gamma_last (decay over the chunk)
   int32_t *chunk_off;                // [N+1] varlen chunk offsets (K0 output)
   int32_t *order;                    // [N] varlen longest-first order (K0 output)
   int32_t *flag;                     // per-call data-error flag (varlen) or null
@@ -43,12 +48,11 @@ struct Problem {
   long long max_chunks;
 };
 
-// TMA descriptors of the token tensors (q, k, the fp16 log-decay la2, v), viewed as
-// 4D [B][T][H][D] (innermost D)
-// with a box of (D or 64 columns) x 1 head x 64 tokens x 1 batch row: one copy per
-// chunk and tensor; tokens past T read as zeros.
+// TMA descriptor of v, viewed as 4D [B][T][H][V] (innermost V) with a box of
+// 64 columns x 1 head x 64 tokens x 1 batch row: one copy per chunk and V slice;
+// tokens past T read as zeros.
 struct TmaMaps {
-  CUtensorMap q, k, la2, v;
+  CUtensorMap v;
 };
 
 struct SeqInfo {

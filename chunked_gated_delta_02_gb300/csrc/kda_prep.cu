@@ -5,22 +5,23 @@
 // 전략의 분리": gate activation, L2 normalisation, decay and the triangular
 // inverse, all parallel over tokens) and the cuLA "kda chunk intra" stage
 // (cuLA launch blog, section "Status & Roadmap"), and hands the recurrence
-// kernel:
-//   * the per-token base-2 log decay la2 = lb log2(e) sigmoid(exp(A_log)(g + dt_bias)),
-//     rounded to fp16 (both kernels use the rounded value);
-//   * one 128 x 64 fp16 matrix per (chunk, head), stored in the 128-byte-swizzled
-//     row order of its shared-memory operand image (so one bulk copy places it):
-//
-//   M = [ -Tb ; P Tb ],   Tb = (I + A)^{-1} diag(beta)
-//   A_ij = beta_i sum_k khat_ik khat_jk 2^{G_ik - G_jk}   (j < i)
-//   P_ij =        sum_k qhat_ik khat_jk 2^{G_ik - G_jk}   (j <= i)
-//
-// with G the in-chunk cumulative base-2 log decay. With M the recurrence kernel
-// forms w = Tb (khat 2^G), u = Tb v, P w and P u as plain products.
+// kernel, per (chunk, head), everything it needs besides v, each in the layout of
+// its shared-memory operand so that one bulk copy places it:
+//   * M = [ -Tb ; P Tb ] (128 x 64 fp16, rows in 128-byte-swizzled order),
+//       Tb = (I + A)^{-1} diag(beta)
+//       A_ij = beta_i sum_k khat_ik khat_jk 2^{G_ik - G_jk}   (j < i)
+//       P_ij =        sum_k qhat_ik khat_jk 2^{G_ik - G_jk}   (j <= i)
+//   * khat Gamma and khat Gamma_last / Gamma (64 x K fp16, MN-major swizzled
+//     images), qhat Gamma (64 x K fp16, row-major) and Gamma_last (K fp32),
+// with G the in-chunk inclusive cumulative base-2 log decay and Gamma = 2^G.
+// With these the recurrence kernel forms w = Tb (khat Gamma), u = Tb v, P w and
+// P u as plain products. The log decay per token and channel is
+// la2 = lb log2(e) sigmoid(exp(A_log)(g + dt_bias)).
 //
 // Norms. khat = k / |k| and qhat = q / |q| are per-row scalings, so they are
-// taken out of the sums: the products run on the raw bf16 values and the read
-// back scales entry (i, j) by beta_i |k_i|^-1 |k_j|^-1 (A) or |q_i|^-1 |k_j|^-1 (P).
+// taken out of the A/P sums: the products run on the raw bf16 values and the
+// read back scales entry (i, j) by beta_i |k_i|^-1 |k_j|^-1 (A) or
+// |q_i|^-1 |k_j|^-1 (P). The norms are computed first, for the hand-off.
 //
 // Exponent range. With lower_bound >= -5 one token decays by at most e^-5, so
 // over 16 tokens |G| <= 80 ln-units (about 115.4 in base 2), which fits in
@@ -82,7 +83,6 @@ struct PrepMisc {
   uint32_t tmem_slot;
   int err;
   float beta[kChunk], kn[kChunk], qn[kChunk];
-  float ksq[2][kChunk], qsq[2][kChunk];   // per half of the channels: row sums of squares
   float2 ssub[4][2][32];                  // per (block, 8-row sub-block, channel pair): sum of la2
 };
 
@@ -164,9 +164,53 @@ prep_kernel(const Problem p) {
     return sm + region + pan * (rows_per_panel * 128) + (uint32_t)row * 128 + (((chk ^ (uint32_t)r) << 4) | sub8);
   };
 
+  // ---- pass 1: row norms |k_i|, |q_i| over all channels (this warp's 8 rows)
+  {
+    float red[16];   // per row: |k|^2 and |q|^2 over this lane's channel pairs
+#pragma unroll
+    for (int r = 0; r < 16; ++r) red[r] = 0.f;
+#pragma unroll
+    for (int hf = 0; hf < K / 64; ++hf) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (r < nrows) {
+          const long long off = rbase + r * rstride + 64 * hf + 2 * lane;
+          const float2 kv = bf2_to_f2(ldg_u32(p.k + off)), qv = bf2_to_f2(ldg_u32(p.q + off));
+          red[r] = fmaf(kv.x, kv.x, fmaf(kv.y, kv.y, red[r]));
+          red[8 + r] = fmaf(qv.x, qv.x, fmaf(qv.y, qv.y, red[8 + r]));
+        }
+      }
+    }
+    // reduce-scatter of the 16 row sums over the warp: after the five steps lane l holds the
+    // full sum of value v(l) = 8 b4 + 4 b3 + 2 b2 + b1 (b = bits of l)
+#pragma unroll
+    for (int w = 8, bit = 16; w >= 1; w >>= 1, bit >>= 1) {
+      const bool up = (lane & bit) != 0;
+#pragma unroll
+      for (int j = 0; j < w; ++j) {
+        const float send = up ? red[j] : red[j + w];
+        const float keep = up ? red[j + w] : red[j];
+        red[j] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+      }
+    }
+    red[0] += __shfl_xor_sync(0xffffffffu, red[0], 1);
+    if ((lane & 1) == 0) {
+      const int v = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+      const int i = row0 + (v & 7);
+      const float nv = (i < len) ? rsqrtf(red[0] + kNormEps) : 0.f;
+      if (v < 8) ms.kn[i] = nv;
+      else ms.qn[i] = nv;
+    }
+  }
+  // per (chunk, head) hand-off slots
+  const long long slot = c * p.H + h;
+  unsigned char *kg_img = reinterpret_cast<unsigned char *>(p.kgimg + slot * (kChunk * K));
+  unsigned char *kt_img = reinterpret_cast<unsigned char *>(p.ktimg + slot * (kChunk * K));
+  __half *qt_out = p.qtb + slot * (kChunk * K);
+
 #pragma unroll 1
   for (int hf = 0; hf < K / 64; ++hf) {
-    // ---- pass 1: gate, log decay to fp16, raw q and k of 8 rows x 2 channels, row norms
+    // ---- pass 2a: gate and log decay of 8 rows x 2 channels
     const int kk = 64 * hf + 2 * lane;
     uint32_t rawk[8], rawq[8], rawg[8];
 #pragma unroll
@@ -184,81 +228,80 @@ prep_kernel(const Problem p) {
     const float2 cdt = make_float2(cg * dt.x, cg * dt.y);
     float2 al[8], kv[8], qv[8];
     float2 ssum = make_float2(0.f, 0.f);
-    float red[16];   // per row: |k|^2 and |q|^2 over this lane's two channels
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       const float2 g2 = bf2_to_f2(rawg[r]);
       const float2 e = __ffma2_rn(make_float2(cg, cg), g2, cdt);
-      const float2 sg = make_float2(rcp_approx(1.f + ex2_approx(e.x)), rcp_approx(1.f + ex2_approx(e.y)));
-      // rounded to fp16 once; this kernel and the recurrence kernel both use the rounded value
-      __half2 la = __floats2half2_rn(lbl2 * sg.x, lbl2 * sg.y);
-      if (r < nrows)
-        *reinterpret_cast<__half2 *>(p.la2 + rbase + r * rstride + kk) = la;
-      else
-        la = __floats2half2_rn(0.f, 0.f);
-      const float2 laf = __half22float2(la);
-      ssum.x += laf.x;
-      ssum.y += laf.y;
-      al[r] = ex2_2(laf);
+      float2 la = make_float2(lbl2 * rcp_approx(1.f + ex2_approx(e.x)), lbl2 * rcp_approx(1.f + ex2_approx(e.y)));
+      if (r >= nrows) la = make_float2(0.f, 0.f);
+      ssum.x += la.x;
+      ssum.y += la.y;
+      al[r] = ex2_2(la);
       kv[r] = bf2_to_f2(rawk[r]);
       qv[r] = bf2_to_f2(rawq[r]);
-      red[r] = kv[r].x * kv[r].x + kv[r].y * kv[r].y;
-      red[8 + r] = qv[r].x * qv[r].x + qv[r].y * qv[r].y;
     }
     ms.ssub[J][sb][lane] = ssum;
-    // reduce-scatter of the 16 row sums over the warp: after the five steps lane l holds the
-    // full sum of value v(l) = 8 b4 + 4 b3 + 2 b2 + b1 (b = bits of l)
-#pragma unroll
-    for (int w = 8, bit = 16; w >= 1; w >>= 1, bit >>= 1) {
-      const bool up = (lane & bit) != 0;
-#pragma unroll
-      for (int j = 0; j < w; ++j) {
-        const float send = up ? red[j] : red[j + w];
-        const float keep = up ? red[j + w] : red[j];
-        red[j] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
-      }
-    }
-    red[0] += __shfl_xor_sync(0xffffffffu, red[0], 1);
-    if ((lane & 1) == 0) {
-      const int v = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-      if (v < 8) ms.ksq[hf][row0 + v] = red[0];
-      else ms.qsq[hf][row0 + v - 8] = red[0];
-    }
     __syncthreads();
 
-    // ---- pass 2: operands of the A/P product for this half (tf32, rounded to nearest)
+    // ---- pass 2b: operands of the A/P product for this half (tf32, rounded to nearest), and the
+    // hand-off khat Gamma, qhat Gamma, khat Gamma_last / Gamma, Gamma_last
+    float2 Bm[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float2 a = ms.ssub[m][0][lane], b = ms.ssub[m][1][lane];
+      Bm[m] = make_float2(a.x + b.x, a.y + b.y);
+    }
     const float2 S0 = ms.ssub[J][0][lane], S1 = ms.ssub[J][1][lane];
-    const float2 BJ = make_float2(S0.x + S1.x, S0.y + S1.y);
+    const float2 BJ = Bm[J];
+    float2 before = make_float2(0.f, 0.f), after = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      if (m < J) before = make_float2(before.x + Bm[m].x, before.y + Bm[m].y);
+      if (m > J) after = make_float2(after.x + Bm[m].x, after.y + Bm[m].y);
+    }
+    const float2 PJ = ex2_2(before), SJ = ex2_2(after);   // decay of the blocks before / after J
+    if (J == 0 && sb == 0) {
+      const float2 tot = make_float2(BJ.x + after.x, BJ.y + after.y);
+      *reinterpret_cast<float2 *>(p.gam + slot * K + kk) = ex2_2(tot);
+    }
+    // byte offset of (row, kk .. kk+1) in a 16-bit MN-major swizzled image (row & 7 == r)
+    const uint32_t img_pan = (uint32_t)hf * 8192u, img_chk = (uint32_t)(lane >> 2), img_sub = (uint32_t)(lane & 3) * 4;
     float2 X = sb ? ex2_2(S0) : make_float2(1.f, 1.f);     // decay from the block start to row0 - 1
     float2 suf = sb ? make_float2(1.f, 1.f) : ex2_2(S1);   // decay over the block rows after the sub-block
     const float2 eBinv = ex2_2(make_float2(-BJ.x, -BJ.y));
     float2 x1 = make_float2(0.f, 0.f), x2 = make_float2(0.f, 0.f);
     if (J == 0) {
-      const float2 a = ms.ssub[1][0][lane], b = ms.ssub[1][1][lane];
-      const float2 c2 = ms.ssub[2][0][lane], d = ms.ssub[2][1][lane];
-      const float2 B1 = make_float2(a.x + b.x, a.y + b.y), B2 = make_float2(c2.x + d.x, c2.y + d.y);
-      x1 = ex2_2(B1);
-      x2 = ex2_2(make_float2(B1.x + B2.x, B1.y + B2.y));
+      x1 = ex2_2(Bm[1]);
+      x2 = ex2_2(make_float2(Bm[1].x + Bm[2].x, Bm[1].y + Bm[2].y));
     } else if (J == 1) {
-      const float2 c2 = ms.ssub[2][0][lane], d = ms.ssub[2][1][lane];
-      x1 = ex2_2(make_float2(c2.x + d.x, c2.y + d.y));
+      x1 = ex2_2(Bm[2]);
     }
     const int xrow = (J == 0) ? 128 : 144;
     if (hf > 0) wait_mma();   // the previous half's product has read the operands
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {   // I side
+    for (int r = 0; r < 8; ++r) {   // I side; Gamma = X 2^{blocks before J}
+      const int i = row0 + r;
       X = mul2(X, al[r]);
-      st_tf32x2(op_at(Lay::opA, 128, row0 + r, r), mul2(kv[r], X));
-      st_tf32x2(op_at(Lay::opA, 128, 64 + row0 + r, r), mul2(qv[r], X));
+      st_tf32x2(op_at(Lay::opA, 128, i, r), mul2(kv[r], X));
+      st_tf32x2(op_at(Lay::opA, 128, 64 + i, r), mul2(qv[r], X));
+      const float2 G = mul2(X, PJ);
+      const float kn = ms.kn[i], qn = ms.qn[i];
+      const uint32_t io = (uint32_t)i * 128u + img_pan + (((img_chk ^ (uint32_t)r) << 4) | img_sub);
+      *reinterpret_cast<__half2 *>(kg_img + io) = __float22half2_rn(mul2(kv[r], mul2(G, make_float2(kn, kn))));
+      *reinterpret_cast<__half2 *>(qt_out + i * K + kk) = __float22half2_rn(mul2(qv[r], mul2(G, make_float2(qn, qn))));
     }
 #pragma unroll
-    for (int r = 7; r >= 0; --r) {  // J side
+    for (int r = 7; r >= 0; --r) {  // J side; Gamma_last / Gamma = Ys 2^{blocks after J}
+      const int i = row0 + r;
       const float2 ys = mul2(kv[r], suf);
       suf = mul2(suf, al[r]);
-      st_tf32x2(op_at(Lay::opB, kOpBRows, row0 + r, r), mul2(ys, eBinv));
-      st_tf32x2(op_at(Lay::opB, kOpBRows, 64 + row0 + r, r), ys);
+      st_tf32x2(op_at(Lay::opB, kOpBRows, i, r), mul2(ys, eBinv));
+      st_tf32x2(op_at(Lay::opB, kOpBRows, 64 + i, r), ys);
       if (J < 2) st_tf32x2(op_at(Lay::opB, kOpBRows, xrow + 8 * sb + r, r), mul2(ys, x1));
       if (J == 0) st_tf32x2(op_at(Lay::opB, kOpBRows, 160 + 8 * sb + r, r), mul2(ys, x2));
+      const float kn = ms.kn[i];
+      const uint32_t io = (uint32_t)i * 128u + img_pan + (((img_chk ^ (uint32_t)r) << 4) | img_sub);
+      *reinterpret_cast<__half2 *>(kt_img + io) = __float22half2_rn(mul2(ys, mul2(SJ, make_float2(kn, kn))));
     }
     umma::fence_proxy_async_smem();
     umma::fence_before_sync();
@@ -277,17 +320,7 @@ prep_kernel(const Problem p) {
     }
   }
 
-  // ---- pass 3: norms, then read A and P back from TMEM (cols 0..175)
-  if (tid < kChunk) {
-    float ks2 = 0.f, qs2 = 0.f;
-#pragma unroll
-    for (int hf = 0; hf < K / 64; ++hf) {
-      ks2 += ms.ksq[hf][tid];
-      qs2 += ms.qsq[hf][tid];
-    }
-    ms.kn[tid] = (tid < len) ? rsqrtf(ks2 + kNormEps) : 0.f;
-    ms.qn[tid] = (tid < len) ? rsqrtf(qs2 + kNormEps) : 0.f;
-  }
+  // ---- pass 3: read A and P back from TMEM (cols 0..175)
   wait_mma();
   __syncthreads();
   // warp w reads TMEM lanes 32 (w % 4) .. + 31 (lane = D row) and the 16-column blocks

@@ -21,12 +21,14 @@
 // delta-rule residuals v - prediction of the chunk; O the inter-chunk term
 // q~ S plus the intra-chunk term P U.
 //
+// The prep kernel hands over M, khat Gamma and k~ (as swizzled operand images),
+// q~ and Gamma_last per chunk; v comes straight from the input by TMA.
+//
 // Warp roles (the S-independent work of chunk n+1 overlaps the state chain of
 // chunk n):
 //   chain group, warps 0-3: D2 += WQ S, U and o, D3 = k~^T U, S update.
-//   prep group, warps 4-11: stages the chunk inputs with TMA, computes
-//     the gate, the decay products and the fp16 operands (one thread per
-//     channel pair and 16-row block), issues D1 and D2, and forms WQ and k~.
+//   prep group, warps 4-11: stages the chunk's operands (bulk copies and one
+//     TMA tile of v), converts v to fp16, issues D1 and D2, and forms WQ.
 // The groups hand over through mbarriers. Every wait gives up after a bounded
 // time; the groups then agree (barrier with OR-reduction) to stop, drain their
 // tensor-core work, free TMEM and report KDA_DEVICE_WAIT_TIMEOUT.
@@ -52,13 +54,10 @@ struct RecLayout {
   static constexpr uint32_t vh = kG + (K / 64) * kPanel64;       // 64 x 64   MN-major (B of D2)
   static constexpr uint32_t WQ = vh + kPanel64;                  // 128 x K   K-major (A of MMA1)
   static constexpr uint32_t Sh = WQ + (K / 64) * 128 * 128;      // K x 64    MN-major (B of MMA1)
-  static constexpr uint32_t kT = Sh + K * 128;                   // 64 x 128  MN-major (A of MMA2)
-  static constexpr uint32_t Uh = kT + 2 * kPanel64;              // 64 x 64   MN-major (B of MMA2)
+  static constexpr uint32_t kT = Sh + K * 128;                   // 2 x (64 x 128 MN-major) (A of MMA2)
+  static constexpr uint32_t Uh = kT + 2 * 2 * kPanel64;          // 64 x 64   MN-major (B of MMA2)
   static constexpr uint32_t qt = Uh + kPanel64;                  // fp16 [64][K] plain
-  static constexpr uint32_t rq = qt + 64 * K * 2;                // raw bf16 q, k, fp16 la2 [64][K], bf16 v [64][64]
-  static constexpr uint32_t rk = rq + 64 * K * 2;
-  static constexpr uint32_t rg = rk + 64 * K * 2;
-  static constexpr uint32_t rv = rg + 64 * K * 2;
+  static constexpr uint32_t rv = qt + 64 * K * 2;                // bf16 v [64][64]
   static constexpr uint32_t misc = rv + 64 * kBV * 2;
   static constexpr uint32_t bytes = misc + 4096 + 1024;          // + misc + alignment slack
 };
@@ -66,11 +65,9 @@ struct RecLayout {
 // Small per-CTA state after the operand buffers.
 template <int K>
 struct RecMisc {
-  uint64_t bar_d12, bar_wq_full, bar_mma1, bar_mma2, bar_exit, bar_in, bar_m;
+  uint64_t bar_d12, bar_wq_full, bar_mma1, bar_mma2, bar_exit, bar_in, bar_q;
   uint32_t tmem_slot;
   int err;
-  float kn[kChunk], qn[kChunk];
-  float btot[4][K];          // per 16-row block and channel: product of alpha over the block
   float gam[2][K];           // per chunk (double-buffered): product of alpha over the chunk
 };
 
@@ -83,15 +80,11 @@ template <int K>
 __global__ void __launch_bounds__(kRecThreads, 1)
 recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   using Lay = RecLayout<K>;
-  constexpr int CPT = K / 64;   // channels per prep thread
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // 1024-byte aligned base, derived from the __shared__ array by pointer arithmetic so that the
   // compiler keeps every access in the shared address space
   unsigned char *sm = smem_raw + ((1024u - (umma::smem_u32(smem_raw) & 1023u)) & 1023u);
   __half *qt = reinterpret_cast<__half *>(sm + Lay::qt);
-  __nv_bfloat16 *rq = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::rq);
-  __nv_bfloat16 *rk = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::rk);
-  __nv_bfloat16 *rg = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::rg);
   __nv_bfloat16 *rv = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::rv);
   RecMisc<K> &ms = *reinterpret_cast<RecMisc<K> *>(sm + Lay::misc);
 
@@ -109,8 +102,8 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   const bool is_chain = warp < 4;
   const int pt = tid - kChainThreads;   // prep thread index (prep group only)
 
-  // ---- set-up: zero the k~ operand (rows >= K stay zero when K = 64), TMEM, barriers
-  for (int x = tid; x < (int)(2 * Lay::kPanel64 / 16); x += kRecThreads)
+  // ---- set-up: zero the k~ operands (rows >= K stay zero when K = 64), TMEM, barriers
+  for (int x = tid; x < (int)(2 * 2 * Lay::kPanel64 / 16); x += kRecThreads)
     reinterpret_cast<uint4 *>(sm + Lay::kT)[x] = make_uint4(0, 0, 0, 0);
   if (warp == 0) {
     umma::tmem_alloc(&ms.tmem_slot, kTmemCols);
@@ -123,7 +116,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
     umma::mbar_init(&ms.bar_mma2, 1);
     umma::mbar_init(&ms.bar_exit, 2);
     umma::mbar_init(&ms.bar_in, 1);
-    umma::mbar_init(&ms.bar_m, 1);
+    umma::mbar_init(&ms.bar_q, 1);
     umma::mbar_fence_init();
     ms.err = 0;
   }
@@ -143,25 +136,29 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       *reinterpret_cast<uint4 *>(sm + Lay::Sh + umma::sw128_chunk(tid, c)) = w;
     }
   }
-  // Inputs of chunk n: one tiled TMA copy per tensor (q, k, g: 64 x K; v: 64 x 64 at column v0),
-  // issued by one prep thread and completing on bar_in. Tokens past T read as zeros; tokens of
-  // the next packed sequence are zeroed after arrival.
-  auto stage_inputs = [&](int n) {
+  // Operands of chunk n, issued by one prep thread, in two groups:
+  //   bar_in: M and khat Gamma (bulk copies of the pre-swizzled images) and the v tile
+  //           (64 x 64 at column v0, one TMA copy; tokens past T read as zeros, tokens of the
+  //           next packed sequence are zeroed after arrival); consumed by D1 / D2.
+  //   bar_q:  q~ (plain), k~ (image, into buffer n & 1) and Gamma_last (into slot n & 1);
+  //           q~ is consumed by the WQ rows, k~ by D3, Gamma_last by the state update.
+  auto stage_in = [&](int n) {
     if (pt == 0) {
-      const int tn = si.t0 + n * kChunk;
-      umma::mbar_arrive_expect_tx(&ms.bar_in, (uint32_t)kChunk * (3 * K * 2 + kBV * 2));
-      umma::tma_load_4d(rq, &maps.q, 0, h, tn, si.b, &ms.bar_in);
-      umma::tma_load_4d(rk, &maps.k, 0, h, tn, si.b, &ms.bar_in);
-      umma::tma_load_4d(rg, &maps.la2, 0, h, tn, si.b, &ms.bar_in);
-      umma::tma_load_4d(rv, &maps.v, v0, h, tn, si.b, &ms.bar_in);
+      const long long slot = ((long long)si.chunk0 + n) * p.H + h;
+      umma::mbar_arrive_expect_tx(&ms.bar_in, 2 * kChunk * kChunk * 2 + kChunk * K * 2 + kChunk * kBV * 2);
+      umma::bulk_g2s(sm + Lay::Mh, p.mats + slot * (2 * kChunk * kChunk), 2 * kChunk * kChunk * 2, &ms.bar_in);
+      umma::bulk_g2s(sm + Lay::kG, p.kgimg + slot * (kChunk * K), kChunk * K * 2, &ms.bar_in);
+      umma::tma_load_4d(rv, &maps.v, v0, h, si.t0 + n * kChunk, si.b, &ms.bar_in);
     }
   };
-  // Hand-off matrix of chunk n: stored pre-swizzled, so one 16 KB bulk copy places it.
-  auto stage_mats = [&](int n) {
+  auto stage_q = [&](int n) {
     if (pt == 0) {
-      umma::mbar_arrive_expect_tx(&ms.bar_m, 2 * kChunk * kChunk * 2);
-      umma::bulk_g2s(sm + Lay::Mh, p.mats + (((long long)si.chunk0 + n) * p.H + h) * (2 * kChunk * kChunk),
-                     2 * kChunk * kChunk * 2, &ms.bar_m);
+      const long long slot = ((long long)si.chunk0 + n) * p.H + h;
+      umma::mbar_arrive_expect_tx(&ms.bar_q, 2 * kChunk * K * 2 + K * 4);
+      umma::bulk_g2s(qt, p.qtb + slot * (kChunk * K), kChunk * K * 2, &ms.bar_q);
+      umma::bulk_g2s(sm + Lay::kT + (n & 1) * (2 * Lay::kPanel64), p.ktimg + slot * (kChunk * K), kChunk * K * 2,
+                     &ms.bar_q);
+      umma::bulk_g2s(&ms.gam[n & 1][0], p.gam + slot * K, K * 4, &ms.bar_q);
     }
   };
   umma::fence_proxy_async_smem();
@@ -169,14 +166,14 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   __syncthreads();
   umma::fence_after_sync();
   if (!is_chain && nch > 0) {
-    stage_inputs(0);
-    stage_mats(0);
+    stage_in(0);
+    stage_q(0);
   }
   const uint32_t tmem = ms.tmem_slot;
   const uint32_t tD1 = tmem, tD3 = tmem + 256;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   bool bad = false;   // this thread saw a wait time out
-  uint32_t in_done = 0, m_done = 0;   // completed bar_in / bar_m phases seen by this thread
+  uint32_t in_done = 0, q_done = 0;   // completed bar_in / bar_q phases seen by this thread
 
   auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
     if (bad) return;
@@ -242,7 +239,8 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
         const uint32_t id = umma::idesc_f16(128, kBV, 1, 1);
 #pragma unroll
         for (int ks = 0; ks < kChunk / 16; ++ks) {
-          const uint64_t a = umma::sdesc_sw128(sbase + Lay::kT + ks * 2048, Lay::kPanel64, 1024);
+          const uint64_t a = umma::sdesc_sw128(sbase + Lay::kT + (n & 1) * (2 * Lay::kPanel64) + ks * 2048,
+                                               Lay::kPanel64, 1024);
           const uint64_t b = umma::sdesc_sw128(sbase + Lay::Uh + ks * 2048, Lay::kPanel64, 1024);
           umma::mma_f16_ss(tD3, a, b, id, ks > 0);
         }
@@ -276,47 +274,19 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
     }
   } else {
     // ======================= prep group =======================
-    const int cg = pt % 64, J = pt / 64;          // channels [cg*CPT, cg*CPT+CPT), rows [16J, 16J+16)
-    const uint32_t col_panel = (uint32_t)((cg * CPT) >> 6) * Lay::kPanel64;
-    const int col_in = (cg * CPT) & 63;
     for (int n = 0; n < nch; ++n) {
       const uint32_t par = (uint32_t)(n & 1);
       const uint32_t tD2 = tmem + 128 + 64 * (n & 1);
       const int L = min(kChunk, si.len - n * kChunk);
       wait_bar(&ms.bar_in, par);
       in_done += bad ? 0u : 1u;
-      if (L < kChunk) {   // rows past the sequence end (next packed sequence or zero fill): zero them
-        for (int x = pt; x < (kChunk - L) * (3 * K + kBV) / 8; x += kPrepGroupThreads) {
-          const int per_row = (3 * K + kBV) / 8, i = L + x / per_row, c = x % per_row;
-          __nv_bfloat16 *dst = (c < K / 8) ? rq + i * K + 8 * c
-                               : (c < 2 * K / 8) ? rk + i * K + 8 * (c - K / 8)
-                               : (c < 3 * K / 8) ? rg + i * K + 8 * (c - 2 * K / 8)
-                                                 : rv + i * kBV + 8 * (c - 3 * K / 8);
-          *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+      if (L < kChunk) {   // v rows past the sequence end (next packed sequence or zero fill): zero them
+        for (int x = pt; x < (kChunk - L) * (kBV / 8); x += kPrepGroupThreads) {
+          const int i = L + x / (kBV / 8), c8 = x % (kBV / 8);
+          *reinterpret_cast<uint4 *>(rv + i * kBV + 8 * c8) = make_uint4(0, 0, 0, 0);
         }
       }
       if (umma::bar_red_or(kBarPrep, kPrepGroupThreads, bad || *(volatile int *)&ms.err != 0)) break;
-      // -- row norms: 4 threads per row, K/4 channels each (bf16x2 from the staged rows)
-      {
-        const int row = pt >> 2, qd = pt & 3;
-        const __nv_bfloat162 *kr = reinterpret_cast<const __nv_bfloat162 *>(rk + row * K) + qd * (K / 8);
-        const __nv_bfloat162 *qr = reinterpret_cast<const __nv_bfloat162 *>(rq + row * K) + qd * (K / 8);
-        float ssk = 0.f, ssq = 0.f;
-#pragma unroll
-        for (int x = 0; x < K / 8; ++x) {
-          const float2 a = __bfloat1622float2(kr[x]), b = __bfloat1622float2(qr[x]);
-          ssk += a.x * a.x + a.y * a.y;
-          ssq += b.x * b.x + b.y * b.y;
-        }
-        ssk += __shfl_xor_sync(0xffffffffu, ssk, 1);
-        ssk += __shfl_xor_sync(0xffffffffu, ssk, 2);
-        ssq += __shfl_xor_sync(0xffffffffu, ssq, 1);
-        ssq += __shfl_xor_sync(0xffffffffu, ssq, 2);
-        if (qd == 0) {
-          ms.kn[row] = (row < L) ? rsqrtf(ssk + kNormEps) : 0.f;
-          ms.qn[row] = (row < L) ? rsqrtf(ssq + kNormEps) : 0.f;
-        }
-      }
       // -- v tile -> fp16 operand (2 chunks of 8 values per thread)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -330,86 +300,9 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
             make_uint4(pack_half2(f0.x, f0.y), pack_half2(f1.x, f1.y), pack_half2(f2.x, f2.y),
                        pack_half2(f3.x, f3.y));
       }
-      // -- per-token decays alpha = 2^la2 of this thread's 16 rows (la2 from the prep kernel)
-      //    and their product over the block (two channels per thread, packed f32x2 arithmetic)
-      float2 al[16], bt = make_float2(1.f, 1.f), pre, suf, kts[16];
-      {
-        const __half *lr = reinterpret_cast<const __half *>(rg);
-        const float2 one = make_float2(1.f, 1.f);
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-          const int i = 16 * J + rr;
-          float2 la;
-          if constexpr (CPT == 2) la = __half22float2(*reinterpret_cast<const __half2 *>(lr + i * K + 2 * cg));
-          else la = make_float2(__half2float(lr[i * K + cg]), 0.f);
-          al[rr] = (i < L) ? make_float2(ex2_approx(la.x), ex2_approx(la.y)) : one;
-          bt = __fmul2_rn(bt, al[rr]);
-        }
-      }
-      ms.btot[J][cg * CPT] = bt.x;
-      if constexpr (CPT == 2) ms.btot[J][cg * CPT + 1] = bt.y;
-      umma::named_bar(kBarPrep, kPrepGroupThreads);   // norms, block products visible
-      // -- decayed operands: kG = khat Gamma and q~ = qhat Gamma (forward), k~ = khat Gamma_last / Gamma
-      {
-        float a[2] = {1.f, 1.f}, b[2] = {1.f, 1.f};
-#pragma unroll
-        for (int e = 0; e < CPT; ++e) {
-          const int c = cg * CPT + e;
-#pragma unroll
-          for (int M = 0; M < 4; ++M) {
-            if (M < J) a[e] *= ms.btot[M][c];
-            if (M > J) b[e] *= ms.btot[M][c];
-          }
-        }
-        pre = make_float2(a[0], a[1]);
-        suf = make_float2(b[0], b[1]);
-        if (J == 0) {
-          ms.gam[n & 1][cg * CPT] = a[0] * bt.x * b[0];
-          if constexpr (CPT == 2) ms.gam[n & 1][cg * CPT + 1] = a[1] * bt.y * b[1];
-        }
-      }
-#pragma unroll
-      for (int rr = 0; rr < 16; ++rr) {
-        const int i = 16 * J + rr;
-        float2 kv, qv;
-        if constexpr (CPT == 2) {
-          kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(rk + i * K + 2 * cg));
-          qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(rq + i * K + 2 * cg));
-        } else {
-          kv = make_float2(__bfloat162float(rk[i * K + cg]), 0.f);
-          qv = make_float2(__bfloat162float(rq[i * K + cg]), 0.f);
-        }
-        const float kn = ms.kn[i], qn = ms.qn[i];
-        pre = __fmul2_rn(pre, al[rr]);
-        const float2 kg = __fmul2_rn(kv, __fmul2_rn(pre, make_float2(kn, kn)));
-        const float2 qq = __fmul2_rn(qv, __fmul2_rn(pre, make_float2(qn, qn)));
-        if constexpr (CPT == 2) {
-          *reinterpret_cast<uint32_t *>(sm + Lay::kG + col_panel + umma::sw128_offset(i, col_in)) =
-              pack_half2(kg.x, kg.y);
-          *reinterpret_cast<uint32_t *>(qt + i * K + cg * CPT) = pack_half2(qq.x, qq.y);
-        } else {
-          *reinterpret_cast<__half *>(sm + Lay::kG + col_panel + umma::sw128_offset(i, col_in)) =
-              __float2half_rn(kg.x);
-          qt[i * K + cg * CPT] = __float2half_rn(qq.x);
-        }
-      }
-#pragma unroll
-      for (int rr = 15; rr >= 0; --rr) {
-        const int i = 16 * J + rr;
-        float2 kv;
-        if constexpr (CPT == 2) kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(rk + i * K + 2 * cg));
-        else kv = make_float2(__bfloat162float(rk[i * K + cg]), 0.f);
-        const float kn = ms.kn[i];
-        kts[rr] = __fmul2_rn(kv, __fmul2_rn(suf, make_float2(kn, kn)));
-        suf = __fmul2_rn(suf, al[rr]);
-      }
       umma::fence_proxy_async_smem();
       umma::fence_before_sync();
-      umma::named_bar(kBarPrep, kPrepGroupThreads);   // kG, vh, qt complete; raw inputs consumed
-      if (pt == 0) {
-        wait_bar(&ms.bar_m, par);
-        m_done += bad ? 0u : 1u;
-      }
+      umma::named_bar(kBarPrep, kPrepGroupThreads);   // vh complete; the v tile is consumed
       if (pt == 0 && !bad) {   // D1 = M (khat Gamma), D2 = M v
         umma::fence_after_sync();
         const uint32_t id1 = umma::idesc_f16(128, K, 0, 1), id2 = umma::idesc_f16(128, kBV, 0, 1);
@@ -423,9 +316,10 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
         }
         umma::commit(&ms.bar_d12);
       }
-      if (n + 1 < nch) stage_inputs(n + 1);   // raw inputs of chunk n are consumed
       wait_bar(&ms.bar_d12, par);
-      if (n + 1 < nch) stage_mats(n + 1);                 // M is consumed by D1/D2
+      if (n + 1 < nch) stage_in(n + 1);   // M, khat Gamma and v of chunk n are consumed
+      wait_bar(&ms.bar_q, par);
+      q_done += bad ? 0u : 1u;
 
       // -- WQ rows: w = -D1 (rows < 64), Q' = q~ - D1 (rows >= 64); WQ must be free (MMA1 of n-1 done)
       if (n > 0) wait_bar(&ms.bar_mma1, par ^ 1u);
@@ -461,23 +355,16 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
           }
         }
       }
-      // -- k~ operand; it must be free (MMA2 of n-1 done)
+      // The k~ buffer of chunk n + 1 was read by D3 of chunk n - 1. Observe that product before
+      // releasing chunk n: afterwards the chain can run ahead and complete another phase.
       if (n > 0) wait_bar(&ms.bar_mma2, par ^ 1u);
-#pragma unroll
-      for (int rr = 0; rr < 16; ++rr) {
-        const int i = 16 * J + rr;
-        if constexpr (CPT == 2) {
-          *reinterpret_cast<uint32_t *>(sm + Lay::kT + col_panel + umma::sw128_offset(i, col_in)) =
-              pack_half2(kts[rr].x, kts[rr].y);
-        } else {
-          *reinterpret_cast<__half *>(sm + Lay::kT + col_panel + umma::sw128_offset(i, col_in)) =
-              __float2half_rn(kts[rr].x);
-        }
-      }
       umma::fence_proxy_async_smem();
       umma::fence_before_sync();
-      umma::named_bar(kBarPrep, kPrepGroupThreads);
-      if (pt == 0 && !bad) umma::mbar_arrive(&ms.bar_wq_full);
+      umma::named_bar(kBarPrep, kPrepGroupThreads);   // WQ complete; q~ consumed
+      if (pt == 0 && !bad) {
+        umma::mbar_arrive(&ms.bar_wq_full);
+        if (n + 1 < nch) stage_q(n + 1);
+      }
     }
   }
 
@@ -490,7 +377,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
     // a copy issued for a chunk that was never processed may still be landing: wait for the
     // next phase of each copy barrier (returns at once if it completes, gives up otherwise)
     umma::mbar_wait_bounded(&ms.bar_in, in_done & 1u, kWaitLimit);
-    if (pt == 0) umma::mbar_wait_bounded(&ms.bar_m, m_done & 1u, kWaitLimit);
+    umma::mbar_wait_bounded(&ms.bar_q, q_done & 1u, kWaitLimit);
   }
   umma::fence_before_sync();
   __syncthreads();

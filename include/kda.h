@@ -77,9 +77,12 @@ typedef enum {
  * Bytes of scratch memory kda_fwd() needs for a problem of this size.
  * num_seqs is the number of sequences N: B without cu_seqlens, the length of
  * cu_seqlens minus one with it. Returns 0 when the sizes are invalid.
- * The scratch holds, per chunk and head, the 128 x 64 fp16 matrix
- * [-(I+A)^{-1} diag(beta); P (I+A)^{-1} diag(beta)] that the prep kernel
- * hands to the recurrence kernel, plus the varlen schedule.
+ * The scratch holds, per chunk and head, what the prep kernel hands to the
+ * recurrence kernel: the 128 x 64 fp16 matrix
+ * [-(I+A)^{-1} diag(beta); P (I+A)^{-1} diag(beta)], the decayed keys and
+ * queries khat Gamma, khat Gamma_last / Gamma and qhat Gamma (fp16, 64 x K
+ * each) and the chunk decay Gamma_last (fp32, K), plus the varlen schedule:
+ * about 64.5 KiB per chunk of 64 tokens and head at K = 128.
  */
 KDA_API size_t kda_fwd_workspace_size(int B, int T, int H, int K, int V, int num_seqs);
 
@@ -109,7 +112,7 @@ KDA_API size_t kda_fwd_workspace_size(int B, int T, int H, int K, int V, int num
  *   stream       the CUDA stream to enqueue on.
  *
  * Alignment: q, k, v, g, o, initial_state and final_state must be 16-byte
- * aligned; beta 2-byte; cu_seqlens, A_log, dt_bias 4-byte. When T == 0 the
+ * aligned; dt_bias 8-byte; beta 2-byte; cu_seqlens, A_log 4-byte. When T == 0 the
  * token tensors (q, k, v, g, beta, o) hold nothing and may be NULL.
  * Returns KDA_OK when the work was enqueued. Concurrent calls on different
  * streams are safe when each has its own workspace and outputs.
@@ -189,7 +192,8 @@ KDA_API kda_status_t kda_debug_chunk_matrices(const void *q, const void *k, cons
  *
  * Limit: the problem must fit in KDA_NOALLOC_MAX_SCRATCH bytes of scratch,
  * i.e. kda_fwd_workspace_size(B, T, H, K, V, num_seqs) <= KDA_NOALLOC_MAX_SCRATCH
- * (about 4 MiB per head per 8192 tokens at K = V = 128: B=1, T=8192 fits H <= 3).
+ * (about 8 MiB per head per 8192 tokens at K = V = 128: B=1, T=8192 fits H = 1,
+ * B=1, T=2048 fits H <= 7).
  * Larger problems are rejected with KDA_ERR_WORKSPACE before anything runs.
  * Every GPU that loads the library holds this array until the process exits.
  *

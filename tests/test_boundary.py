@@ -53,9 +53,11 @@ def test_version_and_strings(lib):
 
 
 def test_workspace_size(lib):
-    # fixed length: B*ceil(T/64) + N chunks, 16 KiB per (chunk, head), plus a small header
+    # fixed length: B*ceil(T/64) + N chunk slots per head; per (chunk, head) the 128 x 64 fp16
+    # matrix, three 64 x K fp16 operands and K fp32 decays, plus a small header
     ws = lib.kda_fwd_workspace_size(2, 2048, 32, 128, 128, 2)
-    assert ws >= (2 * 32 + 2) * 32 * 16384
+    per_slot = 128 * 64 * 2 + 3 * 64 * 128 * 2 + 128 * 4
+    assert (2 * 32 + 2) * 32 * per_slot <= ws <= (2 * 32 + 2) * 32 * per_slot + 5 * 4096
     assert ws % 256 == 0
     assert lib.kda_fwd_workspace_size(0, 10, 1, 64, 64, 0) == 0       # B < 1
     assert lib.kda_fwd_workspace_size(1, -1, 1, 64, 64, 1) == 0       # T < 0
@@ -84,7 +86,7 @@ def _call(lib, **kw):
     (dict(B=0), 1), (dict(T=-1), 1), (dict(H=0), 1), (dict(N=2), 1),
     (dict(cu=FAKE, B=2, N=2), 1),
     (dict(q=FAKE + 8), 1), (dict(o=FAKE + 4), 1), (dict(beta=FAKE + 1), 1), (dict(init=FAKE + 4), 1),
-    (dict(final=FAKE + 8), 1), (dict(cu=FAKE + 2, N=1), 1),
+    (dict(final=FAKE + 8), 1), (dict(cu=FAKE + 2, N=1), 1), (dict(dt_bias=FAKE + 4), 1),
     (dict(ws_bytes=100), 3), (dict(ws=FAKE + 16), 3),
 ])
 def test_host_validation_rejects_without_launch(lib, kw, code):
