@@ -69,11 +69,11 @@ struct PrepLayout {
   static constexpr int LD = 68;                                 // 68 = 4 (mod 32) words: conflict-free rows
   static constexpr uint32_t matA = 0;
   static constexpr uint32_t matT = matA + 64 * LD * 4;
-  static constexpr uint32_t Z = matT + 64 * LD * 4;             // [3][16][17] fp32
+  static constexpr uint32_t Z = matT + 64 * LD * 4;             // [3][16][16] fp32
   static constexpr uint32_t opT = 38 * 1024;                    // Tb^T:     2 panels x  64 rows x 128 B
   static constexpr uint32_t opM = 54 * 1024;                    // [-I ; P]: 2 panels x 128 rows x 128 B
   static constexpr uint32_t end = opM + 2 * 128 * 128;
-  static_assert(Z + 3 * 16 * 17 * 4 <= opT, "A/T/Z overlap the Tb^T operand");
+  static_assert(Z + 3 * 16 * 16 * 4 <= opT, "A/T/Z overlap the Tb^T operand");
   static_assert(opT + 2 * 64 * 128 <= opM, "Tb^T operand overlaps the [-I ; P] operand");
   static_assert(end >= opEnd, "layout end");
 };
@@ -94,9 +94,12 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
 }
 __device__ __forceinline__ float2 ex2_2(float2 x) { return make_float2(ex2_approx(x.x), ex2_approx(x.y)); }
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
-// two tf32-rounded values, stored as one 8-byte word
+// tf32 operands: the tensor core reads the top 19 bits of each 32-bit word and drops the low 13,
+// so adding half a tf32 unit in the last place first makes that truncation round to nearest
+// (ties away from zero) in one integer add.
+__device__ __forceinline__ float tf32_rn(float x) { return __uint_as_float(__float_as_uint(x) + 0x1000u); }
 __device__ __forceinline__ void st_tf32x2(unsigned char *p, float2 v) {
-  *reinterpret_cast<float2 *>(p) = make_float2(to_tf32(v.x), to_tf32(v.y));
+  *reinterpret_cast<float2 *>(p) = make_float2(tf32_rn(v.x), tf32_rn(v.y));
 }
 
 template <int K>
@@ -110,7 +113,7 @@ prep_kernel(const Problem p) {
   PrepMisc &ms = *reinterpret_cast<PrepMisc *>(sm + Lay::end);
   float (*matA)[Lay::LD] = reinterpret_cast<float (*)[Lay::LD]>(sm + Lay::matA);
   float (*matT)[Lay::LD] = reinterpret_cast<float (*)[Lay::LD]>(sm + Lay::matT);
-  float (*Zs)[16][17] = reinterpret_cast<float (*)[16][17]>(sm + Lay::Z);
+  float (*Zs)[16][16] = reinterpret_cast<float (*)[16][16]>(sm + Lay::Z);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long c = blockIdx.x;
@@ -164,21 +167,42 @@ prep_kernel(const Problem p) {
     return sm + region + pan * (rows_per_panel * 128) + (uint32_t)row * 128 + (((chk ^ (uint32_t)r) << 4) | sub8);
   };
 
-  // ---- pass 1: row norms |k_i|, |q_i| over all channels (this warp's 8 rows)
+  // Rows of the sub-block past the sequence end are read from its last valid row (every load is
+  // unconditional, so all of them are in flight at once) and their values are zeroed after.
+  auto row_off = [&](int r) -> long long { return rbase + (long long)min(r, max(nrows - 1, 0)) * rstride; };
+
+  // ---- pass 1: row norms |k_i|, |q_i| over all channels (this warp's 8 rows); g goes to L2 meanwhile
   {
     float red[16];   // per row: |k|^2 and |q|^2 over this lane's channel pairs
 #pragma unroll
     for (int r = 0; r < 16; ++r) red[r] = 0.f;
+    if (nrows > 0) {
+      uint32_t rk[K / 64][8], rq[K / 64][8];
 #pragma unroll
-    for (int hf = 0; hf < K / 64; ++hf) {
+      for (int hf = 0; hf < K / 64; ++hf) {
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        if (r < nrows) {
-          const long long off = rbase + r * rstride + 64 * hf + 2 * lane;
-          const float2 kv = bf2_to_f2(ldg_u32(p.k + off)), qv = bf2_to_f2(ldg_u32(p.q + off));
+        for (int r = 0; r < 8; ++r) {
+          const long long off = row_off(r) + 64 * hf + 2 * lane;
+          rk[hf][r] = ldg_u32(p.k + off);
+          rq[hf][r] = ldg_u32(p.q + off);
+        }
+      }
+      if (lane < 8 * (K / 64)) {   // g of the sub-block to L2: one prefetch per (row, 128-byte line)
+        const int r = lane / (K / 64), line = lane % (K / 64);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.g + row_off(r) + 64 * line));
+      }
+#pragma unroll
+      for (int hf = 0; hf < K / 64; ++hf) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const float2 kv = bf2_to_f2(rk[hf][r]), qv = bf2_to_f2(rq[hf][r]);
           red[r] = fmaf(kv.x, kv.x, fmaf(kv.y, kv.y, red[r]));
           red[8 + r] = fmaf(qv.x, qv.x, fmaf(qv.y, qv.y, red[8 + r]));
         }
+      }
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (r >= nrows) red[r] = red[8 + r] = 0.f;
       }
     }
     // reduce-scatter of the 16 row sums over the warp: after the five steps lane l holds the
@@ -214,13 +238,18 @@ prep_kernel(const Problem p) {
     const int kk = 64 * hf + 2 * lane;
     uint32_t rawk[8], rawq[8], rawg[8];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      rawk[r] = rawq[r] = rawg[r] = 0u;
-      if (r < nrows) {
-        const long long off = rbase + r * rstride + kk;
+    for (int r = 0; r < 8; ++r) rawk[r] = rawq[r] = rawg[r] = 0u;
+    if (nrows > 0) {   // no load at all when the whole sub-block is past the sequence end
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const long long off = row_off(r) + kk;
         rawg[r] = ldg_u32(p.g + off);
         rawk[r] = ldg_u32(p.k + off);
         rawq[r] = ldg_u32(p.q + off);
+      }
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (r >= nrows) rawk[r] = rawq[r] = rawg[r] = 0u;
       }
     }
     float2 dt = make_float2(0.f, 0.f);
@@ -357,25 +386,26 @@ prep_kernel(const Problem p) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float y = (16 * Jb + 4 * q + e < thr) ? x[4 * q + e] * rowf * kj[e] : 0.f;
-          pv[e] = isA ? y : to_tf32(y);
+          pv[e] = isA ? y : tf32_rn(y);
         }
         *reinterpret_cast<float4 *>(rowp + (((c0 + q) ^ xs) << 4)) = v;
       }
     }
   }
-  // the -I half of [-I ; P], and zeros above the block diagonal of A, P and T
+  // the -I half of [-I ; P], and zeros above the block diagonal of P and T, as 16-byte stores of
+  // (row i, 4-column group cq); A above its block diagonal is never read
 #pragma unroll 1
-  for (int x = tid; x < 64 * 64; x += kPrepThreads) {
-    const int i = x >> 6, m = x & 63;
-    auto opM_at = [&](int row, int col) -> float * {
-      return reinterpret_cast<float *>(sm + Lay::opM + (uint32_t)(col >> 5) * (128 * 128) +
-                                       umma::sw128_offset32(row, col & 31));
-    };
-    *opM_at(i, m) = (i == m) ? -1.f : 0.f;
-    if ((m >> 4) > (i >> 4)) {
-      matA[i][m] = 0.f;
-      matT[i][m] = 0.f;
-      *opM_at(64 + i, m) = 0.f;
+  for (int x = tid; x < 64 * 16; x += kPrepThreads) {
+    const int i = x >> 4, cq = x & 15;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    const bool dg = (i >> 2) == cq;   // this group holds the diagonal entry (i, i)
+    const float4 v = make_float4(dg && (i & 3) == 0 ? -1.f : 0.f, dg && (i & 3) == 1 ? -1.f : 0.f,
+                                 dg && (i & 3) == 2 ? -1.f : 0.f, dg && (i & 3) == 3 ? -1.f : 0.f);
+    unsigned char *pan = sm + Lay::opM + (uint32_t)(cq >> 3) * (128 * 128);
+    *reinterpret_cast<float4 *>(pan + umma::sw128_chunk(i, cq & 7)) = v;
+    if (cq >= 4 * ((i >> 4) + 1)) {
+      *reinterpret_cast<float4 *>(pan + umma::sw128_chunk(64 + i, cq & 7)) = z;
+      *reinterpret_cast<float4 *>(&matT[i][4 * cq]) = z;
     }
   }
   __syncthreads();
@@ -398,40 +428,59 @@ prep_kernel(const Problem p) {
     }
   }
   __syncthreads();
-  // ---- pass 4b: off-diagonal blocks, level d = I - J: Z = sum_{J<=M<I} A_IM T_MJ; T_IJ = -T_II Z
+  // ---- pass 4b: off-diagonal blocks, level d = I - J: Z = sum_{J<=M<I} A_IM T_MJ; T_IJ = -T_II Z.
+  // Thread = (block pair, row i, 4-column group c4); 16-byte loads of T and Z rows.
+  auto fma4 = [](float a, const float4 b, float4 &acc) {
+    acc.x = fmaf(a, b.x, acc.x);
+    acc.y = fmaf(a, b.y, acc.y);
+    acc.z = fmaf(a, b.z, acc.z);
+    acc.w = fmaf(a, b.w, acc.w);
+  };
 #pragma unroll 1
   for (int d = 1; d < 4; ++d) {
-    const int npairs = 4 - d;
-#pragma unroll 1
-    for (int x = tid; x < npairs * 256; x += kPrepThreads) {
-      const int Jp = x >> 8, Ip = Jp + d, i = (x >> 4) & 15, col = x & 15;
-      float z[4] = {0.f, 0.f, 0.f, 0.f};
+    const int Jp = tid >> 6, Ip = Jp + d, i = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+    const bool on = Ip < 4;
+    if (on) {
+      float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
       for (int M = Jp; M < Ip; ++M) {
 #pragma unroll
-        for (int m = 0; m < 16; ++m)
-          z[m & 3] = fmaf(matA[16 * Ip + i][16 * M + m], matT[16 * M + m][16 * Jp + col], z[m & 3]);
+        for (int q = 0; q < 4; ++q) {
+          const float4 a = *reinterpret_cast<const float4 *>(&matA[16 * Ip + i][16 * M + 4 * q]);
+          fma4(a.x, *reinterpret_cast<const float4 *>(&matT[16 * M + 4 * q + 0][16 * Jp + c4]), z);
+          fma4(a.y, *reinterpret_cast<const float4 *>(&matT[16 * M + 4 * q + 1][16 * Jp + c4]), z);
+          fma4(a.z, *reinterpret_cast<const float4 *>(&matT[16 * M + 4 * q + 2][16 * Jp + c4]), z);
+          fma4(a.w, *reinterpret_cast<const float4 *>(&matT[16 * M + 4 * q + 3][16 * Jp + c4]), z);
+        }
       }
-      Zs[Jp][i][col] = (z[0] + z[1]) + (z[2] + z[3]);
+      *reinterpret_cast<float4 *>(&Zs[Jp][i][c4]) = z;
     }
     __syncthreads();
-#pragma unroll 1
-    for (int x = tid; x < npairs * 256; x += kPrepThreads) {
-      const int Jp = x >> 8, Ip = Jp + d, i = (x >> 4) & 15, col = x & 15;
-      float t[4] = {0.f, 0.f, 0.f, 0.f};
+    if (on) {
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int m = 0; m < 16; ++m) t[m & 3] = fmaf(matT[16 * Ip + i][16 * Ip + m], Zs[Jp][m][col], t[m & 3]);
-      matT[16 * Ip + i][16 * Jp + col] = -((t[0] + t[1]) + (t[2] + t[3]));
+      for (int q = 0; q < 4; ++q) {
+        const float4 a = *reinterpret_cast<const float4 *>(&matT[16 * Ip + i][16 * Ip + 4 * q]);
+        fma4(a.x, *reinterpret_cast<const float4 *>(&Zs[Jp][4 * q + 0][c4]), t);
+        fma4(a.y, *reinterpret_cast<const float4 *>(&Zs[Jp][4 * q + 1][c4]), t);
+        fma4(a.z, *reinterpret_cast<const float4 *>(&Zs[Jp][4 * q + 2][c4]), t);
+        fma4(a.w, *reinterpret_cast<const float4 *>(&Zs[Jp][4 * q + 3][c4]), t);
+      }
+      *reinterpret_cast<float4 *>(&matT[16 * Ip + i][16 * Jp + c4]) = make_float4(-t.x, -t.y, -t.z, -t.w);
     }
     __syncthreads();
   }
 
   // ---- pass 5: Tb^T operand (row j, column m: T[m][j] beta_j), then M = [-I ; P] Tb on the tensor cores
-#pragma unroll 2
-  for (int x = tid; x < 64 * 64; x += kPrepThreads) {
-    const int m = x >> 6, j = x & 63;   // consecutive threads: consecutive j of one T row
-    *reinterpret_cast<float *>(sm + Lay::opT + (uint32_t)(m >> 5) * (64 * 128) +
-                               umma::sw128_offset32(j, m & 31)) = to_tf32(matT[m][j] * ms.beta[j]);
+  // thread = (row j of Tb^T, 4-column group m4): one 16-byte store per item
+#pragma unroll 1
+  for (int x = tid; x < 64 * 16; x += kPrepThreads) {
+    const int j = x & 63, m4 = 4 * (x >> 6);
+    const float bj = ms.beta[j];
+    const float4 v = make_float4(tf32_rn(matT[m4][j] * bj), tf32_rn(matT[m4 + 1][j] * bj),
+                                 tf32_rn(matT[m4 + 2][j] * bj), tf32_rn(matT[m4 + 3][j] * bj));
+    *reinterpret_cast<float4 *>(sm + Lay::opT + (uint32_t)(m4 >> 5) * (64 * 128) +
+                                umma::sw128_chunk(j, (m4 & 31) >> 2)) = v;
   }
   umma::fence_proxy_async_smem();
   umma::fence_before_sync();
