@@ -36,7 +36,7 @@ struct Problem {
   __half *mats;                      // [max_chunks][H][2C][C] fp16: M = [-Tb ; P Tb]
   __half *kgimg;                     // [max_chunks][H][C x K] fp16: khat Gamma, MN-major image
   __half *ktimg;                     // [max_chunks][H][C x K] fp16: khat Gamma_last / Gamma, MN-major image
-  __half *qtb;                       // [max_chunks][H][C][K] fp16: qhat Gamma, row-major
+  __half *qtb;                       // [max_chunks][H][C x K] fp16: qhat Gamma, image like kgimg
   float *gam;                        // [max_chunks][H][K] fp32: Gamma_last (decay over the chunk)
   int32_t *chunk_off;                // [N+1] varlen chunk offsets (K0 output)
   int32_t *order;                    // [N] varlen longest-first order (K0 output)

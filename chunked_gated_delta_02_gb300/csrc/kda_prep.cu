@@ -11,8 +11,9 @@
 //       Tb = (I + A)^{-1} diag(beta)
 //       A_ij = beta_i sum_k khat_ik khat_jk 2^{G_ik - G_jk}   (j < i)
 //       P_ij =        sum_k qhat_ik khat_jk 2^{G_ik - G_jk}   (j <= i)
-//   * khat Gamma and khat Gamma_last / Gamma (64 x K fp16, MN-major swizzled
-//     images), qhat Gamma (64 x K fp16, row-major) and Gamma_last (K fp32),
+//   * khat Gamma, khat Gamma_last / Gamma and qhat Gamma (64 x K fp16 each, as
+//     images of 64-channel panels of 128-byte swizzled token rows) and
+//     Gamma_last (K fp32),
 // with G the in-chunk inclusive cumulative base-2 log decay and Gamma = 2^G.
 // With these the recurrence kernel forms w = Tb (khat Gamma), u = Tb v, P w and
 // P u as plain products. The log decay per token and channel is
@@ -230,7 +231,7 @@ prep_kernel(const Problem p) {
   const long long slot = c * p.H + h;
   unsigned char *kg_img = reinterpret_cast<unsigned char *>(p.kgimg + slot * (kChunk * K));
   unsigned char *kt_img = reinterpret_cast<unsigned char *>(p.ktimg + slot * (kChunk * K));
-  __half *qt_out = p.qtb + slot * (kChunk * K);
+  unsigned char *qt_img = reinterpret_cast<unsigned char *>(p.qtb + slot * (kChunk * K));
 
 #pragma unroll 1
   for (int hf = 0; hf < K / 64; ++hf) {
@@ -317,7 +318,7 @@ prep_kernel(const Problem p) {
       const float kn = ms.kn[i], qn = ms.qn[i];
       const uint32_t io = (uint32_t)i * 128u + img_pan + (((img_chk ^ (uint32_t)r) << 4) | img_sub);
       *reinterpret_cast<__half2 *>(kg_img + io) = __float22half2_rn(mul2(kv[r], mul2(G, make_float2(kn, kn))));
-      *reinterpret_cast<__half2 *>(qt_out + i * K + kk) = __float22half2_rn(mul2(qv[r], mul2(G, make_float2(qn, qn))));
+      *reinterpret_cast<__half2 *>(qt_img + io) = __float22half2_rn(mul2(qv[r], mul2(G, make_float2(qn, qn))));
     }
 #pragma unroll
     for (int r = 7; r >= 0; --r) {  // J side; Gamma_last / Gamma = Ys 2^{blocks after J}

@@ -56,7 +56,7 @@ struct RecLayout {
   static constexpr uint32_t Sh = WQ + (K / 64) * 128 * 128;      // K x 64    MN-major (B of MMA1)
   static constexpr uint32_t kT = Sh + K * 128;                   // 2 x (64 x 128 MN-major) (A of MMA2)
   static constexpr uint32_t Uh = kT + 2 * 2 * kPanel64;          // 64 x 64   MN-major (B of MMA2)
-  static constexpr uint32_t qt = Uh + kPanel64;                  // fp16 [64][K] plain
+  static constexpr uint32_t qt = Uh + kPanel64;                  // 64 x K    q~ image (64-channel panels)
   static constexpr uint32_t rv = qt + 64 * K * 2;                // bf16 v [64][64]
   static constexpr uint32_t misc = rv + 64 * kBV * 2;
   static constexpr uint32_t bytes = misc + 4096 + 1024;          // + misc + alignment slack
@@ -84,7 +84,6 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   // 1024-byte aligned base, derived from the __shared__ array by pointer arithmetic so that the
   // compiler keeps every access in the shared address space
   unsigned char *sm = smem_raw + ((1024u - (umma::smem_u32(smem_raw) & 1023u)) & 1023u);
-  __half *qt = reinterpret_cast<__half *>(sm + Lay::qt);
   __nv_bfloat16 *rv = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::rv);
   RecMisc<K> &ms = *reinterpret_cast<RecMisc<K> *>(sm + Lay::misc);
 
@@ -140,7 +139,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   //   bar_in: M and khat Gamma (bulk copies of the pre-swizzled images) and the v tile
   //           (64 x 64 at column v0, one TMA copy; tokens past T read as zeros, tokens of the
   //           next packed sequence are zeroed after arrival); consumed by D1 / D2.
-  //   bar_q:  q~ (plain), k~ (image, into buffer n & 1) and Gamma_last (into slot n & 1);
+  //   bar_q:  q~ (image), k~ (image, into buffer n & 1) and Gamma_last (into slot n & 1);
   //           q~ is consumed by the WQ rows, k~ by D3, Gamma_last by the state update.
   auto stage_in = [&](int n) {
     if (pt == 0) {
@@ -155,7 +154,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
     if (pt == 0) {
       const long long slot = ((long long)si.chunk0 + n) * p.H + h;
       umma::mbar_arrive_expect_tx(&ms.bar_q, 2 * kChunk * K * 2 + K * 4);
-      umma::bulk_g2s(qt, p.qtb + slot * (kChunk * K), kChunk * K * 2, &ms.bar_q);
+      umma::bulk_g2s(sm + Lay::qt, p.qtb + slot * (kChunk * K), kChunk * K * 2, &ms.bar_q);
       umma::bulk_g2s(sm + Lay::kT + (n & 1) * (2 * Lay::kPanel64), p.ktimg + slot * (kChunk * K), kChunk * K * 2,
                      &ms.bar_q);
       umma::bulk_g2s(&ms.gam[n & 1][0], p.gam + slot * K, K * 4, &ms.bar_q);
@@ -287,6 +286,14 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
         }
       }
       if (umma::bar_red_or(kBarPrep, kPrepGroupThreads, bad || *(volatile int *)&ms.err != 0)) break;
+      if (pt == 0 && !bad) {   // D1 = M (khat Gamma): both operands arrived by copy
+        umma::fence_after_sync();
+        const uint32_t id1 = umma::idesc_f16(128, K, 0, 1);
+#pragma unroll
+        for (int ks = 0; ks < kChunk / 16; ++ks)
+          umma::mma_f16_ss(tD1, umma::sdesc_sw128(sbase + Lay::Mh + ks * 32, 16, 1024),
+                           umma::sdesc_sw128(sbase + Lay::kG + ks * 2048, Lay::kPanel64, 1024), id1, ks > 0);
+      }
       // -- v tile -> fp16 operand (2 chunks of 8 values per thread)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -303,17 +310,13 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       umma::fence_proxy_async_smem();
       umma::fence_before_sync();
       umma::named_bar(kBarPrep, kPrepGroupThreads);   // vh complete; the v tile is consumed
-      if (pt == 0 && !bad) {   // D1 = M (khat Gamma), D2 = M v
+      if (pt == 0 && !bad) {   // D2 = M v; the commit covers D1 too
         umma::fence_after_sync();
-        const uint32_t id1 = umma::idesc_f16(128, K, 0, 1), id2 = umma::idesc_f16(128, kBV, 0, 1);
+        const uint32_t id2 = umma::idesc_f16(128, kBV, 0, 1);
 #pragma unroll
-        for (int ks = 0; ks < kChunk / 16; ++ks) {
-          const uint64_t a = umma::sdesc_sw128(sbase + Lay::Mh + ks * 32, 16, 1024);
-          umma::mma_f16_ss(tD1, a, umma::sdesc_sw128(sbase + Lay::kG + ks * 2048, Lay::kPanel64, 1024), id1,
-                           ks > 0);
-          umma::mma_f16_ss(tD2, a, umma::sdesc_sw128(sbase + Lay::vh + ks * 2048, Lay::kPanel64, 1024), id2,
-                           ks > 0);
-        }
+        for (int ks = 0; ks < kChunk / 16; ++ks)
+          umma::mma_f16_ss(tD2, umma::sdesc_sw128(sbase + Lay::Mh + ks * 32, 16, 1024),
+                           umma::sdesc_sw128(sbase + Lay::vh + ks * 2048, Lay::kPanel64, 1024), id2, ks > 0);
         umma::commit(&ms.bar_d12);
       }
       wait_bar(&ms.bar_d12, par);
@@ -334,13 +337,19 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
           if (row < kChunk) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) x[j] = -x[j];
-          } else {
-            const __half2 *qr = reinterpret_cast<const __half2 *>(qt + (row - kChunk) * K + c0);
+          } else {   // q~ row (row - 64), columns c0 .. c0 + 15: two swizzled 16-byte chunks
+            const int qi = row - kChunk;
+            const unsigned char *qrow = sm + Lay::qt + (uint32_t)(c0 >> 6) * Lay::kPanel64 + (uint32_t)qi * 128;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float2 f = __half22float2(qr[j]);
-              x[2 * j] = f.x - x[2 * j];
-              x[2 * j + 1] = f.y - x[2 * j + 1];
+            for (int hc = 0; hc < 2; ++hc) {
+              const uint4 raw = *reinterpret_cast<const uint4 *>(qrow + (((((c0 & 63) >> 3) + hc) ^ (qi & 7)) << 4));
+              const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = __half22float2(h2[e]);
+                x[8 * hc + 2 * e] = f.x - x[8 * hc + 2 * e];
+                x[8 * hc + 2 * e + 1] = f.y - x[8 * hc + 2 * e + 1];
+              }
             }
           }
           const uint32_t pan = Lay::WQ + (uint32_t)(c0 >> 6) * (128 * 128);
