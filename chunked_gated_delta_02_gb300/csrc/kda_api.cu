@@ -22,12 +22,11 @@ static __device__ int g_kda_device_status = 0;
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr size_t kMatBytes = 2ull * kda::kChunk * kda::kChunk * sizeof(__half);  // 16 KiB
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t flag_off, chunk_off_off, order_off, mats_off, kg_off, kt_off, qt_off, gam_off, total;
+  size_t flag_off, chunk_off_off, order_off, hand_off, hand_stride, total;
 };
 
 bool sizes_ok(int B, int T, int H, int K, int V, int N) {
@@ -48,17 +47,9 @@ Layout layout_of(int B, int T, int H, int K, int N) {
   L.order_off = off;
   off = align_up(off + sizeof(int32_t) * ((size_t)N + 1));
   const size_t ch = (size_t)max_chunks_of(B, T, N) * (size_t)H;   // (chunk, head) slots
-  const size_t img = (size_t)kda::kChunk * (size_t)K * sizeof(__half);
-  L.mats_off = off;
-  off = align_up(off + ch * kMatBytes);
-  L.kg_off = off;
-  off = align_up(off + ch * img);
-  L.kt_off = off;
-  off = align_up(off + ch * img);
-  L.qt_off = off;
-  off = align_up(off + ch * img);
-  L.gam_off = off;
-  off = align_up(off + ch * (size_t)K * sizeof(float));
+  L.hand_off = off;
+  L.hand_stride = (size_t)kda::hand_bytes(K);
+  off = align_up(off + ch * L.hand_stride);
   L.total = off;
   return L;
 }
@@ -170,11 +161,10 @@ kda_status_t fill_problem(kda::Problem &p, const Layout &L, void *ws, const void
   p.flag = cu ? reinterpret_cast<int32_t *>(base + L.flag_off) : nullptr;
   p.chunk_off = reinterpret_cast<int32_t *>(base + L.chunk_off_off);
   p.order = reinterpret_cast<int32_t *>(base + L.order_off);
-  p.mats = reinterpret_cast<__half *>(base + L.mats_off);
-  p.kgimg = reinterpret_cast<__half *>(base + L.kg_off);
-  p.ktimg = reinterpret_cast<__half *>(base + L.kt_off);
-  p.qtb = reinterpret_cast<__half *>(base + L.qt_off);
-  p.gam = reinterpret_cast<float *>(base + L.gam_off);
+  p.hand = reinterpret_cast<unsigned char *>(base + L.hand_off);
+  p.hand_stride = (long long)L.hand_stride;
+  p.mats = reinterpret_cast<__half *>(p.hand);
+  p.mat_stride = p.hand_stride / 2;
   if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p.dev_status), g_kda_device_status) != cudaSuccess) {
     cudaGetLastError();
     return KDA_ERR_CUDA;
@@ -302,6 +292,7 @@ kda_status_t kda_debug_chunk_matrices(const void *q, const void *k, const void *
   st = fill_problem(p, L, scr.ptr, q, k, k, g, beta, A_log, dt_bias, lower_bound, 1.0f, nullptr, nullptr,
                     cu_seqlens, B, T, H, K, K, num_seqs, nullptr);
   p.mats = static_cast<__half *>(chunk_mats);
+  p.mat_stride = 2 * kda::kChunk * kda::kChunk;
   if (st == KDA_OK && cu_seqlens) st = from_cuda(kda::launch_varlen_schedule(p, s));
   if (st == KDA_OK) st = from_cuda(kda::launch_prep(p, s));
   release_scratch(scr, s);

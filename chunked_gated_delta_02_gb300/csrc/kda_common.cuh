@@ -31,13 +31,13 @@ struct Problem {
   float *final_state;                // [N,H,V,K] or null
   const int32_t *cu;                 // [N+1] or null (fixed length)
   __nv_bfloat16 *o;                  // [B,T,H,V]
-  // prep -> recurrence hand-off, per (chunk, head); the two images are stored in the
-  // 128-byte-swizzled layout of the recurrence kernel's shared-memory operands
-  __half *mats;                      // [max_chunks][H][2C][C] fp16: M = [-Tb ; P Tb]
-  __half *kgimg;                     // [max_chunks][H][C x K] fp16: khat Gamma, MN-major image
-  __half *ktimg;                     // [max_chunks][H][C x K] fp16: khat Gamma_last / Gamma, MN-major image
-  __half *qtb;                       // [max_chunks][H][C x K] fp16: qhat Gamma, image like kgimg
-  float *gam;                        // [max_chunks][H][K] fp32: Gamma_last (decay over the chunk)
+  // prep -> recurrence hand-off: one block per (chunk, head) slot s = chunk * H + head at
+  // hand + s * hand_stride, laid out as described at hand_off_* below; M of slot s is at
+  // mats + s * mat_stride (inside the block, or in a caller buffer for the stage export)
+  unsigned char *hand;
+  long long hand_stride;             // bytes
+  __half *mats;
+  long long mat_stride;              // halves
   int32_t *chunk_off;                // [N+1] varlen chunk offsets (K0 output)
   int32_t *order;                    // [N] varlen longest-first order (K0 output)
   int32_t *flag;                     // per-call data-error flag (varlen) or null
@@ -54,6 +54,22 @@ struct Problem {
 struct TmaMaps {
   CUtensorMap v;
 };
+
+// Hand-off block of one (chunk, head) slot, in bytes. The images are stored in the 128-byte
+// swizzled layout of the recurrence kernel's shared-memory operands (64-channel panels of 64
+// token rows), so bulk copies place them:
+//   [0, 16K)             M = [-Tb ; P Tb], 128 x 64 fp16, rows in swizzled order
+//   [16K, 16K + 128K)    khat Gamma          (64 x K fp16)
+//   next 128K bytes      khat Gamma_last / Gamma
+//   next 128K bytes      qhat Gamma
+//   next 4K bytes        Gamma_last (K fp32)
+// M and khat Gamma are contiguous (one copy), and so are the last three.
+constexpr long long kMatBytes = 2ll * kChunk * kChunk * 2;
+__host__ __device__ constexpr long long hand_off_kg(int K) { return kMatBytes; }
+__host__ __device__ constexpr long long hand_off_kt(int K) { return kMatBytes + 128ll * K; }
+__host__ __device__ constexpr long long hand_off_qt(int K) { return kMatBytes + 256ll * K; }
+__host__ __device__ constexpr long long hand_off_gam(int K) { return kMatBytes + 384ll * K; }
+__host__ __device__ constexpr long long hand_bytes(int K) { return (kMatBytes + 388ll * K + 255) / 256 * 256; }
 
 struct SeqInfo {
   int b;        // batch row

@@ -229,9 +229,8 @@ prep_kernel(const Problem p) {
   }
   // per (chunk, head) hand-off slots
   const long long slot = c * p.H + h;
-  unsigned char *kg_img = reinterpret_cast<unsigned char *>(p.kgimg + slot * (kChunk * K));
-  unsigned char *kt_img = reinterpret_cast<unsigned char *>(p.ktimg + slot * (kChunk * K));
-  unsigned char *qt_img = reinterpret_cast<unsigned char *>(p.qtb + slot * (kChunk * K));
+  unsigned char *hb = p.hand + slot * p.hand_stride;
+  unsigned char *kg_img = hb + hand_off_kg(K), *kt_img = hb + hand_off_kt(K), *qt_img = hb + hand_off_qt(K);
 
 #pragma unroll 1
   for (int hf = 0; hf < K / 64; ++hf) {
@@ -292,7 +291,7 @@ prep_kernel(const Problem p) {
     const float2 PJ = ex2_2(before), SJ = ex2_2(after);   // decay of the blocks before / after J
     if (J == 0 && sb == 0) {
       const float2 tot = make_float2(BJ.x + after.x, BJ.y + after.y);
-      *reinterpret_cast<float2 *>(p.gam + slot * K + kk) = ex2_2(tot);
+      *reinterpret_cast<float2 *>(hb + hand_off_gam(K) + 4 * kk) = ex2_2(tot);
     }
     // byte offset of (row, kk .. kk+1) in a 16-bit MN-major swizzled image (row & 7 == r)
     const uint32_t img_pan = (uint32_t)hf * 8192u, img_chk = (uint32_t)(lane >> 2), img_sub = (uint32_t)(lane & 3) * 4;
@@ -339,13 +338,11 @@ prep_kernel(const Problem p) {
     if (tid == 0) {
       umma::fence_after_sync();
       const uint32_t id = umma::idesc_tf32(128, kOpBRows, 0, 0);
-#pragma unroll 1
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t a = umma::sdesc_sw128(sbase + Lay::opA + (ks >> 2) * (128 * 128) + (ks & 3) * 32, 16, 1024);
-        const uint64_t b =
-            umma::sdesc_sw128(sbase + Lay::opB + (ks >> 2) * (kOpBRows * 128) + (ks & 3) * 32, 16, 1024);
-        umma::mma_tf32_ss(tmem, a, b, id, (hf > 0) || (ks > 0));
-      }
+      const uint64_t a0 = umma::sdesc_sw128(sbase + Lay::opA, 16, 1024), b0 = umma::sdesc_sw128(sbase + Lay::opB, 16, 1024);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        umma::mma_tf32_ss(tmem, umma::desc_add(a0, (ks >> 2) * (128 * 128) + (ks & 3) * 32),
+                          umma::desc_add(b0, (ks >> 2) * (kOpBRows * 128) + (ks & 3) * 32), id, (hf > 0) || (ks > 0));
       umma::commit(&ms.bar);
     }
   }
@@ -489,12 +486,11 @@ prep_kernel(const Problem p) {
   if (tid == 0) {
     umma::fence_after_sync();
     const uint32_t id = umma::idesc_tf32(128, 64, 0, 0);
-#pragma unroll 1
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint64_t a = umma::sdesc_sw128(sbase + Lay::opM + (ks >> 2) * (128 * 128) + (ks & 3) * 32, 16, 1024);
-      const uint64_t b = umma::sdesc_sw128(sbase + Lay::opT + (ks >> 2) * (64 * 128) + (ks & 3) * 32, 16, 1024);
-      umma::mma_tf32_ss(tmem + 192, a, b, id, ks > 0);
-    }
+    const uint64_t a0 = umma::sdesc_sw128(sbase + Lay::opM, 16, 1024), b0 = umma::sdesc_sw128(sbase + Lay::opT, 16, 1024);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      umma::mma_tf32_ss(tmem + 192, umma::desc_add(a0, (ks >> 2) * (128 * 128) + (ks & 3) * 32),
+                        umma::desc_add(b0, (ks >> 2) * (64 * 128) + (ks & 3) * 32), id, ks > 0);
     umma::commit(&ms.bar);
   }
   wait_mma();
@@ -502,7 +498,7 @@ prep_kernel(const Problem p) {
   // warp w takes lanes 32 (w % 4) .. + 31 and columns 32 (w / 4) .. + 31
   {
     const int r = 32 * (warp & 3) + lane;
-    uint4 *dst = reinterpret_cast<uint4 *>(p.mats + ((long long)c * p.H + h) * (2 * kChunk * kChunk)) + r * 8;
+    uint4 *dst = reinterpret_cast<uint4 *>(p.mats + slot * p.mat_stride) + r * 8;
 #pragma unroll 1
     for (int c0 = 32 * (warp >> 2); c0 < 32 * (warp >> 2) + 32; c0 += 16) {
       float x[16];
