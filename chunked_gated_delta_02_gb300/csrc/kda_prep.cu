@@ -350,8 +350,10 @@ prep_kernel(const Problem p) {
   // ---- pass 3: read A and P back from TMEM (cols 0..175)
   wait_mma();
   __syncthreads();
-  // warp w reads TMEM lanes 32 (w % 4) .. + 31 (lane = D row) and the 16-column blocks
-  // cb = w / 4, w / 4 + 2, ... A rows (< 64) go to fp32 matA (times beta_i |k_i|^-1 |k_j|^-1,
+  // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (lane = D row). A lane quadrant holds the row
+  // blocks {0, 1} (quadrants 0, 2) or {2, 3} (quadrants 1, 3), which need the 16-column blocks
+  // {0, 1, 4} or {2, 3, 5, 6, 8, 9, 10}; the two warps of a quadrant split them and load all of
+  // theirs before one wait. A rows (< 64) go to fp32 matA (times beta_i |k_i|^-1 |k_j|^-1,
   // strictly lower), P rows to the [-I ; P] operand (times |q_i|^-1 |k_j|^-1, lower with the
   // diagonal, tf32).
   {
@@ -360,11 +362,19 @@ prep_kernel(const Problem p) {
     const float rowf = isA ? ms.beta[row] * ms.kn[row] : ms.qn[row - 64];
     const int thr = isA ? row : row - 63;   // column j is kept when j < thr
     const int xs = isA ? 0 : (row & 7);
-#pragma unroll 1
-    for (int cb = warp >> 2; cb < kOpBRows / 16; cb += 2) {
-      float x[16];
-      umma::tmem_ld16(tmem + ((uint32_t)(warp & 3) * 32 << 16) + cb * 16, x);
-      umma::tmem_ld_wait();
+    const int sel = (warp & 1) * 2 + (warp >> 2);   // (upper row blocks, second warp of the quadrant)
+    const int cbs[4] = {sel == 0 ? 0 : sel == 1 ? 4 : sel == 2 ? 2 : 6, sel == 0 ? 1 : sel == 2 ? 3 : sel == 3 ? 8 : -1,
+                        sel == 2 ? 5 : sel == 3 ? 9 : -1, sel == 3 ? 10 : -1};
+    float xb[4][16];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (cbs[e] >= 0) umma::tmem_ld16(tmem + ((uint32_t)(warp & 3) * 32 << 16) + cbs[e] * 16, xb[e]);
+    umma::tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int cb = cbs[e];
+      if (cb < 0) continue;
+      const float *x = xb[e];
       // block column Jb of D column block cb for row block I, or -1 if it is not one of row I's
       int Jb = -1;
       if (cb < 4) Jb = (cb == I) ? cb : -1;
@@ -416,7 +426,7 @@ prep_kernel(const Problem p) {
     float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) x[i] = (i == col) ? 1.f : 0.f;
-#pragma unroll 1
+#pragma unroll 4
     for (int j = 0; j < 16; ++j) {
       const float head = x[0];
       matT[o + j][o + col] = head;
