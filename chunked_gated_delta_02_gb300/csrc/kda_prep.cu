@@ -46,8 +46,9 @@
 // Columns 0-63 give the diagonal blocks, 64-127 the blocks next to the
 // diagonal, 128-175 the three blocks further out. The unit lower triangular
 // inverse T = (I + A)^{-1} is blocked: the four 16 x 16 diagonal blocks by
-// forward substitution (one thread per column), then the off-diagonal blocks
-// level by level, T_IJ = -T_II sum_{J<=M<I} A_IM T_MJ, in fp32. Finally
+// forward substitution (one thread per column), then the off-diagonal blocks by
+// doubling, in fp32: the 32 x 32 halves T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22,
+// then the lower-left 32 x 32 block -T_[23] A_[23][01] T_[01]. Finally
 // M = [-I ; P] Tb is a second tensor-core product (128 x 64 x 64).
 #include "kda_common.cuh"
 #include "umma.cuh"
@@ -70,11 +71,11 @@ struct PrepLayout {
   static constexpr int LD = 68;                                 // 68 = 4 (mod 32) words: conflict-free rows
   static constexpr uint32_t matA = 0;
   static constexpr uint32_t matT = matA + 64 * LD * 4;
-  static constexpr uint32_t Z = matT + 64 * LD * 4;             // [3][16][16] fp32
+  static constexpr uint32_t Z = matT + 64 * LD * 4;             // [4][16][16] fp32 merge scratch
   static constexpr uint32_t opT = 38 * 1024;                    // Tb^T:     2 panels x  64 rows x 128 B
   static constexpr uint32_t opM = 54 * 1024;                    // [-I ; P]: 2 panels x 128 rows x 128 B
   static constexpr uint32_t end = opM + 2 * 128 * 128;
-  static_assert(Z + 3 * 16 * 16 * 4 <= opT, "A/T/Z overlap the Tb^T operand");
+  static_assert(Z + 4 * 16 * 16 * 4 <= opT, "A/T/Z overlap the Tb^T operand");
   static_assert(opT + 2 * 64 * 128 <= opM, "Tb^T operand overlaps the [-I ; P] operand");
   static_assert(end >= opEnd, "layout end");
 };
@@ -114,7 +115,7 @@ prep_kernel(const Problem p) {
   PrepMisc &ms = *reinterpret_cast<PrepMisc *>(sm + Lay::end);
   float (*matA)[Lay::LD] = reinterpret_cast<float (*)[Lay::LD]>(sm + Lay::matA);
   float (*matT)[Lay::LD] = reinterpret_cast<float (*)[Lay::LD]>(sm + Lay::matT);
-  float (*Zs)[16][16] = reinterpret_cast<float (*)[16][16]>(sm + Lay::Z);
+  float (*Zs)[16][16] = reinterpret_cast<float (*)[16][16]>(sm + Lay::Z);   // [4][16][16]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long c = blockIdx.x;
@@ -436,45 +437,55 @@ prep_kernel(const Problem p) {
     }
   }
   __syncthreads();
-  // ---- pass 4b: off-diagonal blocks, level d = I - J: Z = sum_{J<=M<I} A_IM T_MJ; T_IJ = -T_II Z.
-  // Thread = (block pair, row i, 4-column group c4); 16-byte loads of T and Z rows.
+  // ---- pass 4b: off-diagonal blocks of T by doubling (four steps). A thread computes a strip of
+  // four columns of one row of a 16 x 16 block with 16-byte loads of T and Z rows.
   auto fma4 = [](float a, const float4 b, float4 &acc) {
     acc.x = fmaf(a, b.x, acc.x);
     acc.y = fmaf(a, b.y, acc.y);
     acc.z = fmaf(a, b.z, acc.z);
     acc.w = fmaf(a, b.w, acc.w);
   };
-#pragma unroll 1
-  for (int d = 1; d < 4; ++d) {
-    const int Jp = tid >> 6, Ip = Jp + d, i = (tid >> 2) & 15, c4 = 4 * (tid & 3);
-    const bool on = Ip < 4;
-    if (on) {
-      float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-      for (int M = Jp; M < Ip; ++M) {
+  // acc += X[xr][xc .. xc + 15] (row of a 16-column block of X) times the 16 x 4 strip of Y
+  // starting at row yr, column yc (Y with leading dimension ldy)
+  auto strip = [&](const float *xrow, const float *y, int ldy, float4 &acc) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 a = *reinterpret_cast<const float4 *>(&matA[16 * Ip + i][16 * M + 4 * q]);
-          fma4(a.x, *reinterpret_cast<const float4 *>(&matT[16 * M + 4 * q + 0][16 * Jp + c4]), z);
-          fma4(a.y, *reinterpret_cast<const float4 *>(&matT[16 * M + 4 * q + 1][16 * Jp + c4]), z);
-          fma4(a.z, *reinterpret_cast<const float4 *>(&matT[16 * M + 4 * q + 2][16 * Jp + c4]), z);
-          fma4(a.w, *reinterpret_cast<const float4 *>(&matT[16 * M + 4 * q + 3][16 * Jp + c4]), z);
-        }
-      }
-      *reinterpret_cast<float4 *>(&Zs[Jp][i][c4]) = z;
+    for (int q = 0; q < 4; ++q) {
+      const float4 a = *reinterpret_cast<const float4 *>(xrow + 4 * q);
+      fma4(a.x, *reinterpret_cast<const float4 *>(y + (4 * q + 0) * ldy), acc);
+      fma4(a.y, *reinterpret_cast<const float4 *>(y + (4 * q + 1) * ldy), acc);
+      fma4(a.z, *reinterpret_cast<const float4 *>(y + (4 * q + 2) * ldy), acc);
+      fma4(a.w, *reinterpret_cast<const float4 *>(y + (4 * q + 3) * ldy), acc);
+    }
+  };
+  {
+    const int i = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+    // level 1, blocks (I, I - 1) for I = 1, 3: Z = A_{I,I-1} T_{I-1,I-1}, then T_{I,I-1} = -T_II Z
+    const int p1 = tid >> 6, I1 = 2 * p1 + 1;   // threads 0..127
+    if (tid < 128) {
+      float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      strip(&matA[16 * I1 + i][16 * (I1 - 1)], &matT[16 * (I1 - 1)][16 * (I1 - 1) + c4], Lay::LD, z);
+      *reinterpret_cast<float4 *>(&Zs[p1][i][c4]) = z;
     }
     __syncthreads();
-    if (on) {
+    if (tid < 128) {
       float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 a = *reinterpret_cast<const float4 *>(&matT[16 * Ip + i][16 * Ip + 4 * q]);
-        fma4(a.x, *reinterpret_cast<const float4 *>(&Zs[Jp][4 * q + 0][c4]), t);
-        fma4(a.y, *reinterpret_cast<const float4 *>(&Zs[Jp][4 * q + 1][c4]), t);
-        fma4(a.z, *reinterpret_cast<const float4 *>(&Zs[Jp][4 * q + 2][c4]), t);
-        fma4(a.w, *reinterpret_cast<const float4 *>(&Zs[Jp][4 * q + 3][c4]), t);
-      }
-      *reinterpret_cast<float4 *>(&matT[16 * Ip + i][16 * Jp + c4]) = make_float4(-t.x, -t.y, -t.z, -t.w);
+      strip(&matT[16 * I1 + i][16 * I1], &Zs[p1][0][c4], 16, t);
+      *reinterpret_cast<float4 *>(&matT[16 * I1 + i][16 * (I1 - 1) + c4]) = make_float4(-t.x, -t.y, -t.z, -t.w);
+    }
+    __syncthreads();
+    // level 2, the lower-left 32 x 32 block (row blocks a = 2, 3; column blocks b = 0, 1):
+    // Z_ab = sum_{b <= c <= 1} A_ac T_cb, then T_ab = -sum_{2 <= c <= a} T_ac Z_cb
+    const int a = 2 + (tid >> 7), b = (tid >> 6) & 1;
+    {
+      float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = b; c <= 1; ++c) strip(&matA[16 * a + i][16 * c], &matT[16 * c][16 * b + c4], Lay::LD, z);
+      *reinterpret_cast<float4 *>(&Zs[2 * (a - 2) + b][i][c4]) = z;
+    }
+    __syncthreads();
+    {
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = 2; c <= a; ++c) strip(&matT[16 * a + i][16 * c], &Zs[2 * (c - 2) + b][0][c4], 16, t);
+      *reinterpret_cast<float4 *>(&matT[16 * a + i][16 * b + c4]) = make_float4(-t.x, -t.y, -t.z, -t.w);
     }
     __syncthreads();
   }
