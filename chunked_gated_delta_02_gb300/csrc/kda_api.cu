@@ -105,7 +105,7 @@ kda_status_t check_common(const void *q, const void *k, const void *g, const voi
     return KDA_ERR_INVALID_ARG;
   }
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(g, 16) || !aligned(beta, 2) ||
-      !aligned(A_log, 4) || (dt_bias && !aligned(dt_bias, 8)))
+      !aligned(A_log, 4) || (dt_bias && !aligned(dt_bias, 16)))
     return KDA_ERR_INVALID_ARG;
   // element counts must fit the 64-bit index arithmetic of the kernels
   const double elems = (double)B * (double)T * (double)H * (double)K;

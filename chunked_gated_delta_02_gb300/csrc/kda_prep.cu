@@ -85,7 +85,7 @@ struct PrepMisc {
   uint32_t tmem_slot;
   int err;
   float beta[kChunk], kn[kChunk], qn[kChunk];
-  float2 ssub[4][2][32];                  // per (block, 8-row sub-block, channel pair): sum of la2
+  float4 ssub[4][4][16];                  // per (block, 4-row sub-block, channel quad): sum of la2
 };
 
 __device__ __forceinline__ uint32_t ldg_u32(const __nv_bfloat16 *p) {
@@ -100,8 +100,26 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a
 // so adding half a tf32 unit in the last place first makes that truncation round to nearest
 // (ties away from zero) in one integer add.
 __device__ __forceinline__ float tf32_rn(float x) { return __uint_as_float(__float_as_uint(x) + 0x1000u); }
-__device__ __forceinline__ void st_tf32x2(unsigned char *p, float2 v) {
-  *reinterpret_cast<float2 *>(p) = make_float2(tf32_rn(v.x), tf32_rn(v.y));
+// Four channels of one row, as two packed pairs.
+struct F4 {
+  float2 lo, hi;
+};
+__device__ __forceinline__ F4 mul4(F4 a, F4 b) { return {__fmul2_rn(a.lo, b.lo), __fmul2_rn(a.hi, b.hi)}; }
+__device__ __forceinline__ F4 add4(F4 a, F4 b) { return {__fadd2_rn(a.lo, b.lo), __fadd2_rn(a.hi, b.hi)}; }
+__device__ __forceinline__ F4 ex2_4(F4 x) { return {ex2_2(x.lo), ex2_2(x.hi)}; }
+__device__ __forceinline__ F4 splat4(float v) { return {make_float2(v, v), make_float2(v, v)}; }
+__device__ __forceinline__ F4 f4_of(float4 v) { return {make_float2(v.x, v.y), make_float2(v.z, v.w)}; }
+__device__ __forceinline__ float4 float4_of(F4 v) { return make_float4(v.lo.x, v.lo.y, v.hi.x, v.hi.y); }
+__device__ __forceinline__ F4 bf4_to_f4(uint2 u) { return {bf2_to_f2(u.x), bf2_to_f2(u.y)}; }
+__device__ __forceinline__ uint2 ldg_u64(const __nv_bfloat16 *p) { return __ldg(reinterpret_cast<const uint2 *>(p)); }
+// four tf32-rounded values, one 16-byte store
+__device__ __forceinline__ void st_tf32x4(unsigned char *p, F4 v) {
+  *reinterpret_cast<float4 *>(p) = make_float4(tf32_rn(v.lo.x), tf32_rn(v.lo.y), tf32_rn(v.hi.x), tf32_rn(v.hi.y));
+}
+// four fp16 values, one 8-byte store
+__device__ __forceinline__ void st_half4(unsigned char *p, F4 v) {
+  const __half2 a = __float22half2_rn(v.lo), b = __float22half2_rn(v.hi);
+  *reinterpret_cast<uint2 *>(p) = make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
 }
 
 template <int K>
@@ -153,64 +171,68 @@ prep_kernel(const Problem p) {
     umma::fence_after_sync();
   };
 
-  // Elementwise unit of this thread: channel pair `lane` of the current half, 16-row block
-  // J = warp / 2, 8-row sub-block sb = warp % 2.
-  const int J = warp >> 1, sb = warp & 1;
-  const int row0 = 16 * J + 8 * sb;
-  const int nrows = max(0, min(8, len - row0));
+  // Elementwise unit of this thread: channel quad cq = lane % 16 of the current half (channels
+  // 4 cq .. 4 cq + 3) and the 4-row sub-block sb4 = 2 warp + lane / 16 (rows 4 sb4 .. + 3), which
+  // is sub-block sbi = sb4 % 4 of the 16-row block J = sb4 / 4. A warp covers two rows of 64
+  // channels, so every global access of a row is one 128-byte line.
+  const int cq = lane & 15, sb4 = 2 * warp + (lane >> 4), J = sb4 >> 2, sbi = sb4 & 3;
+  const int row0 = 4 * sb4;
+  const int nrows = max(0, min(4, len - row0));
   const float ea = expf(p.A_log[h]);
   const float cg = -ea * kLog2e;                 // sigmoid(a) = 1 / (1 + 2^{cg (g + dt)})
   const float lbl2 = p.lb * kLog2e;
   const long long rstride = (long long)p.H * K;  // elements between consecutive tokens
   const long long rbase = tok_row(p, si.b, t0 + row0, h) * K;
-  // swizzled byte offset of this lane's channel pair inside a row (row & 7 == r for row0 + r)
-  const uint32_t pan = (uint32_t)(lane >> 4), chk = (uint32_t)((lane & 15) >> 1), sub8 = (uint32_t)(lane & 1) * 8;
+  const uint32_t r7 = (uint32_t)(sb4 & 1) << 2;  // (row0 + r) & 7 == r7 + r
+  // tf32 operand (32 channels per 128-byte row): this quad is one 16-byte chunk
   auto op_at = [&](uint32_t region, uint32_t rows_per_panel, int row, int r) -> unsigned char * {
-    return sm + region + pan * (rows_per_panel * 128) + (uint32_t)row * 128 + (((chk ^ (uint32_t)r) << 4) | sub8);
+    return sm + region + (uint32_t)(cq >> 3) * (rows_per_panel * 128) + (uint32_t)row * 128 +
+           ((((uint32_t)cq & 7u) ^ (r7 + (uint32_t)r)) << 4);
   };
 
   // Rows of the sub-block past the sequence end are read from its last valid row (every load is
   // unconditional, so all of them are in flight at once) and their values are zeroed after.
   auto row_off = [&](int r) -> long long { return rbase + (long long)min(r, max(nrows - 1, 0)) * rstride; };
 
-  // ---- pass 1: row norms |k_i|, |q_i| over all channels (this warp's 8 rows); g goes to L2 meanwhile
+  // ---- pass 1: row norms |k_i|, |q_i| over all channels (this thread's 4 rows); g goes to L2 meanwhile
   {
-    float red[16];   // per row: |k|^2 and |q|^2 over this lane's channel pairs
+    float red[8];   // per row: |k|^2 (0..3) and |q|^2 (4..7) over this lane's channel quads
 #pragma unroll
-    for (int r = 0; r < 16; ++r) red[r] = 0.f;
+    for (int r = 0; r < 8; ++r) red[r] = 0.f;
     if (nrows > 0) {
-      uint32_t rk[K / 64][8], rq[K / 64][8];
+      uint2 rk[K / 64][4], rq[K / 64][4];
 #pragma unroll
       for (int hf = 0; hf < K / 64; ++hf) {
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const long long off = row_off(r) + 64 * hf + 2 * lane;
-          rk[hf][r] = ldg_u32(p.k + off);
-          rq[hf][r] = ldg_u32(p.q + off);
+        for (int r = 0; r < 4; ++r) {
+          const long long off = row_off(r) + 64 * hf + 4 * cq;
+          rk[hf][r] = ldg_u64(p.k + off);
+          rq[hf][r] = ldg_u64(p.q + off);
         }
       }
-      if (lane < 8 * (K / 64)) {   // g of the sub-block to L2: one prefetch per (row, 128-byte line)
-        const int r = lane / (K / 64), line = lane % (K / 64);
+      if (cq < 4 * (K / 64)) {   // g of the sub-block to L2: one prefetch per (row, 128-byte line)
+        const int r = cq / (K / 64), line = cq % (K / 64);
         asm volatile("prefetch.global.L2 [%0];" ::"l"(p.g + row_off(r) + 64 * line));
       }
 #pragma unroll
       for (int hf = 0; hf < K / 64; ++hf) {
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const float2 kv = bf2_to_f2(rk[hf][r]), qv = bf2_to_f2(rq[hf][r]);
-          red[r] = fmaf(kv.x, kv.x, fmaf(kv.y, kv.y, red[r]));
-          red[8 + r] = fmaf(qv.x, qv.x, fmaf(qv.y, qv.y, red[8 + r]));
+        for (int r = 0; r < 4; ++r) {
+          const F4 kv = bf4_to_f4(rk[hf][r]), qv = bf4_to_f4(rq[hf][r]);
+          red[r] = fmaf(kv.lo.x, kv.lo.x, fmaf(kv.lo.y, kv.lo.y, fmaf(kv.hi.x, kv.hi.x, fmaf(kv.hi.y, kv.hi.y, red[r]))));
+          red[4 + r] =
+              fmaf(qv.lo.x, qv.lo.x, fmaf(qv.lo.y, qv.lo.y, fmaf(qv.hi.x, qv.hi.x, fmaf(qv.hi.y, qv.hi.y, red[4 + r]))));
         }
       }
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        if (r >= nrows) red[r] = red[8 + r] = 0.f;
+      for (int r = 0; r < 4; ++r) {
+        if (r >= nrows) red[r] = red[4 + r] = 0.f;
       }
     }
-    // reduce-scatter of the 16 row sums over the warp: after the five steps lane l holds the
-    // full sum of value v(l) = 8 b4 + 4 b3 + 2 b2 + b1 (b = bits of l)
+    // reduce-scatter of the 8 row sums over the 16 lanes of this sub-block: after the four steps
+    // lane l holds the full sum of value v(l) = 4 b3 + 2 b2 + b1 (b = bits of l)
 #pragma unroll
-    for (int w = 8, bit = 16; w >= 1; w >>= 1, bit >>= 1) {
+    for (int w = 4, bit = 8; w >= 1; w >>= 1, bit >>= 1) {
       const bool up = (lane & bit) != 0;
 #pragma unroll
       for (int j = 0; j < w; ++j) {
@@ -221,10 +243,10 @@ prep_kernel(const Problem p) {
     }
     red[0] += __shfl_xor_sync(0xffffffffu, red[0], 1);
     if ((lane & 1) == 0) {
-      const int v = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-      const int i = row0 + (v & 7);
+      const int v = ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+      const int i = row0 + (v & 3);
       const float nv = (i < len) ? rsqrtf(red[0] + kNormEps) : 0.f;
-      if (v < 8) ms.kn[i] = nv;
+      if (v < 4) ms.kn[i] = nv;
       else ms.qn[i] = nv;
     }
   }
@@ -235,103 +257,103 @@ prep_kernel(const Problem p) {
 
 #pragma unroll 1
   for (int hf = 0; hf < K / 64; ++hf) {
-    // ---- pass 2a: gate and log decay of 8 rows x 2 channels
-    const int kk = 64 * hf + 2 * lane;
-    uint32_t rawk[8], rawq[8], rawg[8];
+    // ---- pass 2a: gate and log decay of 4 rows x 4 channels
+    const int kk = 64 * hf + 4 * cq;
+    uint2 rawk[4], rawq[4], rawg[4];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) rawk[r] = rawq[r] = rawg[r] = 0u;
+    for (int r = 0; r < 4; ++r) rawk[r] = rawq[r] = rawg[r] = make_uint2(0u, 0u);
     if (nrows > 0) {   // no load at all when the whole sub-block is past the sequence end
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
+      for (int r = 0; r < 4; ++r) {
         const long long off = row_off(r) + kk;
-        rawg[r] = ldg_u32(p.g + off);
-        rawk[r] = ldg_u32(p.k + off);
-        rawq[r] = ldg_u32(p.q + off);
+        rawg[r] = ldg_u64(p.g + off);
+        rawk[r] = ldg_u64(p.k + off);
+        rawq[r] = ldg_u64(p.q + off);
       }
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        if (r >= nrows) rawk[r] = rawq[r] = rawg[r] = 0u;
+      for (int r = 0; r < 4; ++r) {
+        if (r >= nrows) rawk[r] = rawq[r] = rawg[r] = make_uint2(0u, 0u);
       }
     }
-    float2 dt = make_float2(0.f, 0.f);
-    if (p.dt_bias) dt = *reinterpret_cast<const float2 *>(p.dt_bias + h * K + kk);
-    const float2 cdt = make_float2(cg * dt.x, cg * dt.y);
-    float2 al[8], kv[8], qv[8];
-    float2 ssum = make_float2(0.f, 0.f);
+    F4 dt = splat4(0.f);
+    if (p.dt_bias) dt = f4_of(*reinterpret_cast<const float4 *>(p.dt_bias + h * K + kk));
+    const F4 cdt = mul4(splat4(cg), dt);
+    F4 al[4], kv[4], qv[4];
+    F4 ssum = splat4(0.f);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const float2 g2 = bf2_to_f2(rawg[r]);
-      const float2 e = __ffma2_rn(make_float2(cg, cg), g2, cdt);
-      float2 la = make_float2(lbl2 * rcp_approx(1.f + ex2_approx(e.x)), lbl2 * rcp_approx(1.f + ex2_approx(e.y)));
-      if (r >= nrows) la = make_float2(0.f, 0.f);
-      ssum.x += la.x;
-      ssum.y += la.y;
-      al[r] = ex2_2(la);
-      kv[r] = bf2_to_f2(rawk[r]);
-      qv[r] = bf2_to_f2(rawq[r]);
+    for (int r = 0; r < 4; ++r) {
+      const F4 g4 = bf4_to_f4(rawg[r]);
+      const F4 e = {__ffma2_rn(make_float2(cg, cg), g4.lo, cdt.lo), __ffma2_rn(make_float2(cg, cg), g4.hi, cdt.hi)};
+      F4 la = {make_float2(lbl2 * rcp_approx(1.f + ex2_approx(e.lo.x)), lbl2 * rcp_approx(1.f + ex2_approx(e.lo.y))),
+               make_float2(lbl2 * rcp_approx(1.f + ex2_approx(e.hi.x)), lbl2 * rcp_approx(1.f + ex2_approx(e.hi.y)))};
+      if (r >= nrows) la = splat4(0.f);
+      ssum = add4(ssum, la);
+      al[r] = ex2_4(la);
+      kv[r] = bf4_to_f4(rawk[r]);
+      qv[r] = bf4_to_f4(rawq[r]);
     }
-    ms.ssub[J][sb][lane] = ssum;
+    ms.ssub[J][sbi][cq] = float4_of(ssum);
     __syncthreads();
 
     // ---- pass 2b: operands of the A/P product for this half (tf32, rounded to nearest), and the
     // hand-off khat Gamma, qhat Gamma, khat Gamma_last / Gamma, Gamma_last
-    float2 Bm[4];
+    F4 Bm[4], Xs = splat4(0.f), Ss = splat4(0.f), BJ = splat4(0.f), before = splat4(0.f), after = splat4(0.f);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      const float2 a = ms.ssub[m][0][lane], b = ms.ssub[m][1][lane];
-      Bm[m] = make_float2(a.x + b.x, a.y + b.y);
-    }
-    const float2 S0 = ms.ssub[J][0][lane], S1 = ms.ssub[J][1][lane];
-    const float2 BJ = Bm[J];
-    float2 before = make_float2(0.f, 0.f), after = make_float2(0.f, 0.f);
+      F4 bsum = splat4(0.f);
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      if (m < J) before = make_float2(before.x + Bm[m].x, before.y + Bm[m].y);
-      if (m > J) after = make_float2(after.x + Bm[m].x, after.y + Bm[m].y);
+      for (int q = 0; q < 4; ++q) {
+        const F4 v = f4_of(ms.ssub[m][q][cq]);
+        bsum = add4(bsum, v);
+        if (m == J && q < sbi) Xs = add4(Xs, v);
+        if (m == J && q > sbi) Ss = add4(Ss, v);
+      }
+      Bm[m] = bsum;
+      if (m == J) BJ = bsum;
+      if (m < J) before = add4(before, bsum);
+      if (m > J) after = add4(after, bsum);
     }
-    const float2 PJ = ex2_2(before), SJ = ex2_2(after);   // decay of the blocks before / after J
-    if (J == 0 && sb == 0) {
-      const float2 tot = make_float2(BJ.x + after.x, BJ.y + after.y);
-      *reinterpret_cast<float2 *>(hb + hand_off_gam(K) + 4 * kk) = ex2_2(tot);
-    }
-    // byte offset of (row, kk .. kk+1) in a 16-bit MN-major swizzled image (row & 7 == r)
-    const uint32_t img_pan = (uint32_t)hf * 8192u, img_chk = (uint32_t)(lane >> 2), img_sub = (uint32_t)(lane & 3) * 4;
-    float2 X = sb ? ex2_2(S0) : make_float2(1.f, 1.f);     // decay from the block start to row0 - 1
-    float2 suf = sb ? make_float2(1.f, 1.f) : ex2_2(S1);   // decay over the block rows after the sub-block
-    const float2 eBinv = ex2_2(make_float2(-BJ.x, -BJ.y));
-    float2 x1 = make_float2(0.f, 0.f), x2 = make_float2(0.f, 0.f);
+    const F4 PJ = ex2_4(before), SJ = ex2_4(after);   // decay of the blocks before / after J
+    if (J == 0 && sbi == 0)
+      *reinterpret_cast<float4 *>(hb + hand_off_gam(K) + 4 * kk) = float4_of(ex2_4(add4(BJ, after)));
+    // byte offset of (row, kk .. kk + 3) in a 16-bit image of 64-channel panels (row & 7 == r7 + r)
+    auto img_off = [&](int r) -> uint32_t {
+      return (uint32_t)(row0 + r) * 128u + (uint32_t)hf * 8192u +
+             (((((uint32_t)cq >> 1) ^ (r7 + (uint32_t)r)) << 4) | (((uint32_t)cq & 1u) << 3));
+    };
+    F4 X = ex2_4(Xs);     // decay from the block start to row0 - 1
+    F4 suf = ex2_4(Ss);   // decay over the block rows after the sub-block
+    const F4 eBinv = ex2_4({make_float2(-BJ.lo.x, -BJ.lo.y), make_float2(-BJ.hi.x, -BJ.hi.y)});
+    F4 x1 = splat4(0.f), x2 = splat4(0.f);
     if (J == 0) {
-      x1 = ex2_2(Bm[1]);
-      x2 = ex2_2(make_float2(Bm[1].x + Bm[2].x, Bm[1].y + Bm[2].y));
+      x1 = ex2_4(Bm[1]);
+      x2 = ex2_4(add4(Bm[1], Bm[2]));
     } else if (J == 1) {
-      x1 = ex2_2(Bm[2]);
+      x1 = ex2_4(Bm[2]);
     }
-    const int xrow = (J == 0) ? 128 : 144;
+    const int xrow = ((J == 0) ? 128 : 144) + 4 * sbi, yrow = 160 + 4 * sbi;
     if (hf > 0) wait_mma();   // the previous half's product has read the operands
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {   // I side; Gamma = X 2^{blocks before J}
+    for (int r = 0; r < 4; ++r) {   // I side; Gamma = X 2^{blocks before J}
       const int i = row0 + r;
-      X = mul2(X, al[r]);
-      st_tf32x2(op_at(Lay::opA, 128, i, r), mul2(kv[r], X));
-      st_tf32x2(op_at(Lay::opA, 128, 64 + i, r), mul2(qv[r], X));
-      const float2 G = mul2(X, PJ);
-      const float kn = ms.kn[i], qn = ms.qn[i];
-      const uint32_t io = (uint32_t)i * 128u + img_pan + (((img_chk ^ (uint32_t)r) << 4) | img_sub);
-      *reinterpret_cast<__half2 *>(kg_img + io) = __float22half2_rn(mul2(kv[r], mul2(G, make_float2(kn, kn))));
-      *reinterpret_cast<__half2 *>(qt_img + io) = __float22half2_rn(mul2(qv[r], mul2(G, make_float2(qn, qn))));
+      X = mul4(X, al[r]);
+      st_tf32x4(op_at(Lay::opA, 128, i, r), mul4(kv[r], X));
+      st_tf32x4(op_at(Lay::opA, 128, 64 + i, r), mul4(qv[r], X));
+      const F4 G = mul4(X, PJ);
+      const uint32_t io = img_off(r);
+      st_half4(kg_img + io, mul4(kv[r], mul4(G, splat4(ms.kn[i]))));
+      st_half4(qt_img + io, mul4(qv[r], mul4(G, splat4(ms.qn[i]))));
     }
 #pragma unroll
-    for (int r = 7; r >= 0; --r) {  // J side; Gamma_last / Gamma = Ys 2^{blocks after J}
+    for (int r = 3; r >= 0; --r) {  // J side; Gamma_last / Gamma = Ys 2^{blocks after J}
       const int i = row0 + r;
-      const float2 ys = mul2(kv[r], suf);
-      suf = mul2(suf, al[r]);
-      st_tf32x2(op_at(Lay::opB, kOpBRows, i, r), mul2(ys, eBinv));
-      st_tf32x2(op_at(Lay::opB, kOpBRows, 64 + i, r), ys);
-      if (J < 2) st_tf32x2(op_at(Lay::opB, kOpBRows, xrow + 8 * sb + r, r), mul2(ys, x1));
-      if (J == 0) st_tf32x2(op_at(Lay::opB, kOpBRows, 160 + 8 * sb + r, r), mul2(ys, x2));
-      const float kn = ms.kn[i];
-      const uint32_t io = (uint32_t)i * 128u + img_pan + (((img_chk ^ (uint32_t)r) << 4) | img_sub);
-      *reinterpret_cast<__half2 *>(kt_img + io) = __float22half2_rn(mul2(ys, mul2(SJ, make_float2(kn, kn))));
+      const F4 ys = mul4(kv[r], suf);
+      suf = mul4(suf, al[r]);
+      st_tf32x4(op_at(Lay::opB, kOpBRows, i, r), mul4(ys, eBinv));
+      st_tf32x4(op_at(Lay::opB, kOpBRows, 64 + i, r), ys);
+      if (J < 2) st_tf32x4(op_at(Lay::opB, kOpBRows, xrow + r, r), mul4(ys, x1));
+      if (J == 0) st_tf32x4(op_at(Lay::opB, kOpBRows, yrow + r, r), mul4(ys, x2));
+      st_half4(kt_img + img_off(r), mul4(ys, mul4(SJ, splat4(ms.kn[i]))));
     }
     umma::fence_proxy_async_smem();
     umma::fence_before_sync();

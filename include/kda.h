@@ -112,7 +112,7 @@ KDA_API size_t kda_fwd_workspace_size(int B, int T, int H, int K, int V, int num
  *   stream       the CUDA stream to enqueue on.
  *
  * Alignment: q, k, v, g, o, initial_state and final_state must be 16-byte
- * aligned; dt_bias 8-byte; beta 2-byte; cu_seqlens, A_log 4-byte. When T == 0 the
+ * aligned; dt_bias 16-byte; beta 2-byte; cu_seqlens, A_log 4-byte. When T == 0 the
  * token tensors (q, k, v, g, beta, o) hold nothing and may be NULL.
  * Returns KDA_OK when the work was enqueued. Concurrent calls on different
  * streams are safe when each has its own workspace and outputs.

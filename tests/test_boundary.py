@@ -86,7 +86,7 @@ def _call(lib, **kw):
     (dict(B=0), 1), (dict(T=-1), 1), (dict(H=0), 1), (dict(N=2), 1),
     (dict(cu=FAKE, B=2, N=2), 1),
     (dict(q=FAKE + 8), 1), (dict(o=FAKE + 4), 1), (dict(beta=FAKE + 1), 1), (dict(init=FAKE + 4), 1),
-    (dict(final=FAKE + 8), 1), (dict(cu=FAKE + 2, N=1), 1), (dict(dt_bias=FAKE + 4), 1),
+    (dict(final=FAKE + 8), 1), (dict(cu=FAKE + 2, N=1), 1), (dict(dt_bias=FAKE + 4), 1), (dict(dt_bias=FAKE + 8), 1),
     (dict(ws_bytes=100), 3), (dict(ws=FAKE + 16), 3),
 ])
 def test_host_validation_rejects_without_launch(lib, kw, code):
