@@ -33,6 +33,7 @@ SIGNATURES = {
     "kda_max_chunks": (ctypes.c_int64, [I, I, I]),
     "kda_status_string": (ctypes.c_char_p, [I]),
     "kda_get_device_status": (I, [P, ctypes.POINTER(ctypes.c_int)]),
+    "kda_debug_wait_timeout": (I, [ctypes.c_longlong, P]),
     "kda_version": (I, []),
 }
 

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/kda.h: argument validation,
 // workspace layout, and the K0 -> K1 -> K2 launch sequence on one stream.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cmath>
 #include <cstdint>
@@ -9,6 +10,7 @@
 
 #include "../../include/kda.h"
 #include "kda_common.cuh"
+#include "umma.cuh"
 
 namespace kda {
 cudaError_t launch_varlen_schedule(const Problem &p, cudaStream_t stream);
@@ -18,6 +20,24 @@ cudaError_t launch_recur(const Problem &p, const TmaMaps &maps, cudaStream_t str
 
 // Sticky per-device data-error word (KDA_DEVICE_* codes).
 static __device__ int g_kda_device_status = 0;
+
+// One bounded wait on an mbarrier that nothing arrives on (see kda_debug_wait_timeout).
+static __global__ void wait_timeout_kernel(long long limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    kda::umma::mbar_init(&bar, 1);
+    kda::umma::mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !kda::umma::mbar_wait_bounded(&bar, 0, limit))
+    atomicExch(&g_kda_device_status, kda::kDevWaitTimeout);
+}
+
+// NVTX range for the host-side enqueue of one stage (shows up around the launches in a trace).
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 namespace {
 
@@ -251,16 +271,31 @@ kda_status_t kda_fwd_with_events(const void *q, const void *k, const void *v, co
     if (st == KDA_OK && ev) st = from_cuda(cudaEventRecord(static_cast<cudaEvent_t>(ev), s));
   };
   mark(events ? events->prep_start : nullptr);
-  if (st == KDA_OK && cu_seqlens) st = from_cuda(kda::launch_varlen_schedule(p, s));
-  if (st == KDA_OK) st = from_cuda(kda::launch_prep(p, s));
+  if (st == KDA_OK && cu_seqlens) {
+    NvtxRange r("kda K0 varlen schedule");
+    st = from_cuda(kda::launch_varlen_schedule(p, s));
+  }
+  if (st == KDA_OK) {
+    NvtxRange r("kda K1 prep");
+    st = from_cuda(kda::launch_prep(p, s));
+  }
   mark(events ? events->prep_done : nullptr);
   kda::TmaMaps maps;
   std::memset(&maps, 0, sizeof maps);
   if (st == KDA_OK && T > 0 && !encode_token_map(&maps.v, v, V, H, T, B, 64)) st = KDA_ERR_CUDA;
-  if (st == KDA_OK) st = from_cuda(kda::launch_recur(p, maps, s));
+  if (st == KDA_OK) {
+    NvtxRange r("kda K2 recurrence");
+    st = from_cuda(kda::launch_recur(p, maps, s));
+  }
   mark(events ? events->recur_done : nullptr);
   release_scratch(scr, s);
   return st;
+}
+
+kda_status_t kda_debug_wait_timeout(long long limit_cycles, kda_stream_t stream) {
+  if (limit_cycles < 1 || limit_cycles >= (1ll << 32)) return KDA_ERR_INVALID_ARG;
+  wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_cycles);
+  return from_cuda(cudaGetLastError());
 }
 
 kda_status_t kda_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,

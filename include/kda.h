@@ -228,6 +228,18 @@ KDA_API const char *kda_status_string(kda_status_t status);
  */
 KDA_API kda_status_t kda_get_device_status(kda_stream_t stream, int *device_code);
 
+/*
+ * Exercises the failure path of the pipeline kernels' bounded waits. One CTA
+ * waits on an mbarrier that nothing arrives on, with the same bounded wait the
+ * kernels use, for about limit_cycles SM clocks; it then records
+ * KDA_DEVICE_WAIT_TIMEOUT in the device status word, exactly as a kernel whose
+ * wait gave up does, and exits. Nothing faults or hangs and the context stays
+ * usable; kda_get_device_status() then reports the code.
+ * limit_cycles must be in [1, 2^32). Returns KDA_OK when the launch was
+ * enqueued, KDA_ERR_INVALID_ARG for a limit out of range, KDA_ERR_CUDA.
+ */
+KDA_API kda_status_t kda_debug_wait_timeout(long long limit_cycles, kda_stream_t stream);
+
 /* Library version as major*10000 + minor*100 + patch. */
 KDA_API int kda_version(void);
 

@@ -101,3 +101,9 @@ def test_null_token_tensors_allowed_only_when_empty(lib):
 def test_zero_sequences_is_a_no_op(lib):
     # N = 0 packed sequences: nothing to do, no CUDA call is made
     assert _call(lib, cu=FAKE, N=0, T=0) == 0
+
+
+def test_debug_wait_timeout_rejects_bad_limits_without_launch(lib):
+    assert lib.kda_debug_wait_timeout(0, None) == 1
+    assert lib.kda_debug_wait_timeout(-5, None) == 1
+    assert lib.kda_debug_wait_timeout(1 << 32, None) == 1

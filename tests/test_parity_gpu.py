@@ -150,3 +150,54 @@ def test_full_size_sampled(name):
     assert bool(torch.isfinite(o.float()).all()) and bool(torch.isfinite(fs).all())
     eo, mo, es = check_pairs(inp, o, fs, FULL[name], name)
     print(f"{name}: o rel {eo:.2e} maxabs {mo:.2e} state rel {es:.2e}")
+
+
+def test_bounded_wait_timeout_is_reported_and_context_survives():
+    """A wait that nothing releases gives up after its bound, records KDA_DEVICE_WAIT_TIMEOUT in
+    the device status word (as a pipeline kernel's wait does), and leaves the context usable."""
+    import chunked_gated_delta_02_gb300 as kda
+    from chunked_gated_delta_02_gb300._lib import lib
+    kda.device_status()                     # clear any earlier record
+    assert lib().kda_debug_wait_timeout(2_000_000, None) == 0    # about a millisecond of SM clocks
+    assert kda.device_status() == 2
+    assert kda.device_status() == 0         # read-and-clear
+    inp = make_inputs(named("tiny"), seed=0)
+    ref_o, ref_f = oracle_full(inp)
+    o, fs = run_gpu(inp)
+    assert_parity(o, fs, ref_o, ref_f, "after a timeout")
+    assert kda.device_status() == 0
+
+
+GUARD = 4096   # guard bytes before and after each buffer
+
+
+def _guarded(nbytes, fill):
+    """A device buffer of nbytes with GUARD bytes of `fill` on both sides; returns (whole, view)."""
+    whole = torch.full((GUARD + nbytes + GUARD,), fill, dtype=torch.uint8, device="cuda")
+    return whole, whole[GUARD:GUARD + nbytes]
+
+
+@pytest.mark.parametrize("w", [custom(B=2, T=300, H=3, K=128, V=128, init_state=True),
+                               custom(H=2, K=64, V=64, seqlens=[0, 70, 1, 129], init_state=True)],
+                         ids=["fixed", "varlen-K64"])
+def test_writes_stay_inside_workspace_and_outputs(w):
+    """Canary bytes around the workspace, o and final_state are unchanged by a call that uses
+    exactly the workspace size the library asks for."""
+    import chunked_gated_delta_02_gb300 as kda
+    inp = make_inputs(w, seed=31)
+    d = to_dev(inp)
+    B, T, H, K, V, N = (inp[x] for x in ("B", "T", "H", "K", "V", "N"))
+    need = kda.workspace_size(B, T, H, K, V, N)
+    ws_whole, ws = _guarded(need, 0xA5)
+    o_whole, o_bytes = _guarded(B * T * H * V * 2, 0x5A)
+    f_whole, f_bytes = _guarded(N * H * V * K * 4, 0x3C)
+    o = o_bytes.view(torch.bfloat16).view(B, T, H, V)
+    fs = f_bytes.view(torch.float32).view(N, H, V, K)
+    kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"], d["lower_bound"],
+            d["scale"], d["initial_state"], True, d["cu_seqlens"], workspace=ws, out=o, final_state=fs)
+    torch.cuda.synchronize()
+    for name, whole, fill in (("workspace", ws_whole, 0xA5), ("o", o_whole, 0x5A), ("final_state", f_whole, 0x3C)):
+        assert bool((whole[:GUARD] == fill).all()), f"{name}: bytes before the buffer changed"
+        assert bool((whole[-GUARD:] == fill).all()), f"{name}: bytes after the buffer changed"
+    ref_o, ref_f = oracle_full(inp)
+    assert_parity(o, fs, ref_o, ref_f, "guarded buffers")
