@@ -184,15 +184,27 @@ prep_kernel(const Problem p) {
   const long long rstride = (long long)p.H * K;  // elements between consecutive tokens
   const long long rbase = tok_row(p, si.b, t0 + row0, h) * K;
   const uint32_t r7 = (uint32_t)(sb4 & 1) << 2;  // (row0 + r) & 7 == r7 + r
-  // tf32 operand (32 channels per 128-byte row): this quad is one 16-byte chunk
-  auto op_at = [&](uint32_t region, uint32_t rows_per_panel, int row, int r) -> unsigned char * {
-    return sm + region + (uint32_t)(cq >> 3) * (rows_per_panel * 128) + (uint32_t)row * 128 +
-           ((((uint32_t)cq & 7u) ^ (r7 + (uint32_t)r)) << 4);
-  };
+  // Swizzled byte offsets of this thread's quad in its rows, computed once:
+  //   tf32 operand (32 channels per 128-byte row): the quad is one 16-byte chunk;
+  //   16-bit image (64 channels per 128-byte row): the quad is half a chunk.
+  uint32_t op_x[4], img_x[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    op_x[r] = (uint32_t)(row0 + r) * 128u + ((((uint32_t)cq & 7u) ^ (r7 + (uint32_t)r)) << 4);
+    img_x[r] = (uint32_t)(row0 + r) * 128u + (((((uint32_t)cq >> 1) ^ (r7 + (uint32_t)r)) << 4) | (((uint32_t)cq & 1u) << 3));
+  }
+  unsigned char *const opA_q = sm + Lay::opA + (uint32_t)(cq >> 3) * (128 * 128);
+  unsigned char *const opB_q = sm + Lay::opB + (uint32_t)(cq >> 3) * (kOpBRows * 128);
+  // operand row `base + row0 + r` (base a multiple of 8) of this thread's quad
+  auto opA_at = [&](int base, int r) -> unsigned char * { return opA_q + (uint32_t)base * 128u + op_x[r]; };
+  auto opB_at = [&](int base, int r) -> unsigned char * { return opB_q + (uint32_t)base * 128u + op_x[r]; };
 
   // Rows of the sub-block past the sequence end are read from its last valid row (every load is
   // unconditional, so all of them are in flight at once) and their values are zeroed after.
-  auto row_off = [&](int r) -> long long { return rbase + (long long)min(r, max(nrows - 1, 0)) * rstride; };
+  long long roff[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) roff[r] = rbase + (long long)min(r, max(nrows - 1, 0)) * rstride;
+  auto row_off = [&](int r) -> long long { return roff[r]; };
 
   // ---- pass 1: row norms |k_i|, |q_i| over all channels (this thread's 4 rows); g goes to L2 meanwhile
   {
@@ -212,7 +224,7 @@ prep_kernel(const Problem p) {
       }
       if (cq < 4 * (K / 64)) {   // g of the sub-block to L2: one prefetch per (row, 128-byte line)
         const int r = cq / (K / 64), line = cq % (K / 64);
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.g + row_off(r) + 64 * line));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.g + rbase + (long long)min(r, nrows - 1) * rstride + 64 * line));
       }
 #pragma unroll
       for (int hf = 0; hf < K / 64; ++hf) {
@@ -316,11 +328,8 @@ prep_kernel(const Problem p) {
     const F4 PJ = ex2_4(before), SJ = ex2_4(after);   // decay of the blocks before / after J
     if (J == 0 && sbi == 0)
       *reinterpret_cast<float4 *>(hb + hand_off_gam(K) + 4 * kk) = float4_of(ex2_4(add4(BJ, after)));
-    // byte offset of (row, kk .. kk + 3) in a 16-bit image of 64-channel panels (row & 7 == r7 + r)
-    auto img_off = [&](int r) -> uint32_t {
-      return (uint32_t)(row0 + r) * 128u + (uint32_t)hf * 8192u +
-             (((((uint32_t)cq >> 1) ^ (r7 + (uint32_t)r)) << 4) | (((uint32_t)cq & 1u) << 3));
-    };
+    // byte offset of (row0 + r, kk .. kk + 3) in a 16-bit image of 64-channel panels
+    auto img_off = [&](int r) -> uint32_t { return (uint32_t)hf * 8192u + img_x[r]; };
     F4 X = ex2_4(Xs);     // decay from the block start to row0 - 1
     F4 suf = ex2_4(Ss);   // decay over the block rows after the sub-block
     const F4 eBinv = ex2_4({make_float2(-BJ.lo.x, -BJ.lo.y), make_float2(-BJ.hi.x, -BJ.hi.y)});
@@ -337,8 +346,8 @@ prep_kernel(const Problem p) {
     for (int r = 0; r < 4; ++r) {   // I side; Gamma = X 2^{blocks before J}
       const int i = row0 + r;
       X = mul4(X, al[r]);
-      st_tf32x4(op_at(Lay::opA, 128, i, r), mul4(kv[r], X));
-      st_tf32x4(op_at(Lay::opA, 128, 64 + i, r), mul4(qv[r], X));
+      st_tf32x4(opA_at(0, r), mul4(kv[r], X));
+      st_tf32x4(opA_at(64, r), mul4(qv[r], X));
       const F4 G = mul4(X, PJ);
       const uint32_t io = img_off(r);
       st_half4(kg_img + io, mul4(kv[r], mul4(G, splat4(ms.kn[i]))));
@@ -349,10 +358,10 @@ prep_kernel(const Problem p) {
       const int i = row0 + r;
       const F4 ys = mul4(kv[r], suf);
       suf = mul4(suf, al[r]);
-      st_tf32x4(op_at(Lay::opB, kOpBRows, i, r), mul4(ys, eBinv));
-      st_tf32x4(op_at(Lay::opB, kOpBRows, 64 + i, r), ys);
-      if (J < 2) st_tf32x4(op_at(Lay::opB, kOpBRows, xrow + r, r), mul4(ys, x1));
-      if (J == 0) st_tf32x4(op_at(Lay::opB, kOpBRows, yrow + r, r), mul4(ys, x2));
+      st_tf32x4(opB_at(0, r), mul4(ys, eBinv));
+      st_tf32x4(opB_at(64, r), ys);
+      if (J < 2) st_tf32x4(opB_at(xrow - row0, r), mul4(ys, x1));
+      if (J == 0) st_tf32x4(opB_at(yrow - row0, r), mul4(ys, x2));
       st_half4(kt_img + img_off(r), mul4(ys, mul4(SJ, splat4(ms.kn[i]))));
     }
     umma::fence_proxy_async_smem();
