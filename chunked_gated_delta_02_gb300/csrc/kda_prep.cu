@@ -450,22 +450,27 @@ prep_kernel(const Problem p) {
   }
   __syncthreads();
 
-  // ---- pass 4a: diagonal blocks of T by forward substitution (thread = (block, column)). The
-  // column lives in a shift register: at step j the head x[0] is final (T row j), and x[s] then
-  // takes the update of row j + 1 + s.
-  if (tid < kChunk) {
-    const int Jd = tid >> 4, col = tid & 15, o = 16 * Jd;
-    float x[16];
+  // ---- pass 4a: diagonal blocks of T by forward substitution. Thread = (column of a diagonal
+  // block, quarter of its rows): column c = tid / 4 of block Jd = c / 16, rows 4 qr .. 4 qr + 3 of
+  // the block in registers. At step j the thread holding row j shares it with its column's
+  // other three threads (one shuffle), which update their rows below j.
+  {
+    const int cix = tid >> 2, qr = tid & 3;
+    const int Jd = cix >> 4, col = cix & 15, o = 16 * Jd;
+    float x[4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = (i == col) ? 1.f : 0.f;
-#pragma unroll 4
+    for (int s2 = 0; s2 < 4; ++s2) x[s2] = (4 * qr + s2 == col) ? 1.f : 0.f;
+#pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const float head = x[0];
-      matT[o + j][o + col] = head;
-      const float *aj = &matA[o + j][o + j];
+      const float xj = __shfl_sync(0xffffffffu, x[j & 3], (lane & ~3) | (j >> 2));
 #pragma unroll
-      for (int s2 = 1; s2 < 16; ++s2) x[s2 - 1] = fmaf((j + s2 < 16) ? -aj[s2 * Lay::LD] : 0.f, head, x[s2]);
+      for (int s2 = 0; s2 < 4; ++s2) {
+        const int i = 4 * qr + s2;
+        if (i > j) x[s2] = fmaf(-matA[o + i][o + j], xj, x[s2]);
+      }
     }
+#pragma unroll
+    for (int s2 = 0; s2 < 4; ++s2) matT[o + 4 * qr + s2][o + col] = x[s2];
   }
   __syncthreads();
   // ---- pass 4b: off-diagonal blocks of T by doubling (four steps). A thread computes a strip of
