@@ -60,14 +60,14 @@ struct TmaMaps {
 // token rows), so bulk copies place them:
 //   [0, 16K)             M = [-Tb ; P Tb], 128 x 64 fp16, rows in swizzled order
 //   [16K, 16K + 128K)    khat Gamma          (64 x K fp16)
-//   next 128K bytes      khat Gamma_last / Gamma
 //   next 128K bytes      qhat Gamma
+//   next 128K bytes      khat Gamma_last / Gamma
 //   next 4K bytes        Gamma_last (K fp32)
-// M and khat Gamma are contiguous (one copy), and so are the last three.
+// M and khat Gamma are contiguous (one copy), and so are the last two.
 constexpr long long kMatBytes = 2ll * kChunk * kChunk * 2;
 __host__ __device__ constexpr long long hand_off_kg(int K) { return kMatBytes; }
-__host__ __device__ constexpr long long hand_off_kt(int K) { return kMatBytes + 128ll * K; }
-__host__ __device__ constexpr long long hand_off_qt(int K) { return kMatBytes + 256ll * K; }
+__host__ __device__ constexpr long long hand_off_qt(int K) { return kMatBytes + 128ll * K; }
+__host__ __device__ constexpr long long hand_off_kt(int K) { return kMatBytes + 256ll * K; }
 __host__ __device__ constexpr long long hand_off_gam(int K) { return kMatBytes + 384ll * K; }
 __host__ __device__ constexpr long long hand_bytes(int K) { return (kMatBytes + 388ll * K + 255) / 256 * 256; }
 
