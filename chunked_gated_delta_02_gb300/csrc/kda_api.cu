@@ -15,7 +15,8 @@
 namespace kda {
 cudaError_t launch_varlen_schedule(const Problem &p, cudaStream_t stream);
 cudaError_t launch_prep(const Problem &p, cudaStream_t stream);
-cudaError_t launch_recur(const Problem &p, const TmaMaps &maps, cudaStream_t stream);
+cudaError_t launch_recur(const Problem &p, const TmaMaps &maps, int bv, cudaStream_t stream);
+int recur_slice_width(const Problem &p);
 }  // namespace kda
 
 // Sticky per-device data-error word (KDA_DEVICE_* codes).
@@ -282,10 +283,11 @@ kda_status_t kda_fwd_with_events(const void *q, const void *k, const void *v, co
   mark(events ? events->prep_done : nullptr);
   kda::TmaMaps maps;
   std::memset(&maps, 0, sizeof maps);
-  if (st == KDA_OK && T > 0 && !encode_token_map(&maps.v, v, V, H, T, B, 64)) st = KDA_ERR_CUDA;
+  const int bv = kda::recur_slice_width(p);
+  if (st == KDA_OK && T > 0 && !encode_token_map(&maps.v, v, V, H, T, B, bv)) st = KDA_ERR_CUDA;
   if (st == KDA_OK) {
     NvtxRange r("kda K2 recurrence");
-    st = from_cuda(kda::launch_recur(p, maps, s));
+    st = from_cuda(kda::launch_recur(p, maps, bv, s));
   }
   mark(events ? events->recur_done : nullptr);
   release_scratch(scr, s);

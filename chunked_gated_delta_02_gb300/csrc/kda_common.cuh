@@ -49,8 +49,8 @@ struct Problem {
 };
 
 // TMA descriptor of v, viewed as 4D [B][T][H][V] (innermost V) with a box of
-// 64 columns x 1 head x 64 tokens x 1 batch row: one copy per chunk and V slice;
-// tokens past T read as zeros.
+// (V-slice width) columns x 1 head x 64 tokens x 1 batch row: one copy per chunk and
+// V slice; tokens past T read as zeros.
 struct TmaMaps {
   CUtensorMap v;
 };

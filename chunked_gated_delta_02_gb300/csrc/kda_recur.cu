@@ -46,14 +46,17 @@ namespace kda {
 constexpr int kChainThreads = 128;
 constexpr int kSubThreads = 128;                              // one prep sub-group
 constexpr int kRecThreads = kChainThreads + 2 * kSubThreads;
-constexpr int kBV = 64;
+// V slice per CTA: 64 columns, or 16 when 64-column slices would leave most SMs idle (few long
+// sequences); the operand panels keep their 64-column rows and a narrow slice uses their first
+// columns.
+constexpr int kBVWide = 64, kBVNarrow = 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clocks per wait
 // named barrier ids (0 is __syncthreads): the chain, and prep sub-groups 0 and 1
 constexpr int kBarChain = 1;
 __device__ __forceinline__ int sub_bar(int sg) { return 2 + sg; }
 
-template <int K>
+template <int K, int BV>
 struct RecLayout {
   // byte offsets from the 1024-aligned dynamic shared memory base
   static constexpr uint32_t kPanel64 = 64 * 128;                 // 64 rows x 128 B
@@ -64,8 +67,8 @@ struct RecLayout {
   static constexpr uint32_t mk_kg = 128 * 128, mk_vh = mk_kg + (K / 64) * kPanel64, mk_size = mk_vh + kPanel64;
   static constexpr uint32_t Sh = mk + 2 * mk_size;               // K x 64    MN-major (B of MMA1)
   static constexpr uint32_t Uh = Sh + K * 128;                   // 64 x 64   MN-major (B of MMA2)
-  static constexpr uint32_t rv = Uh + kPanel64;                  // per parity: bf16 v [64][64]
-  static constexpr uint32_t qt = rv + 2 * 64 * kBV * 2;          // per parity: q~ image (64 x K)
+  static constexpr uint32_t rv = Uh + kPanel64;                  // per parity: bf16 v [64][BV]
+  static constexpr uint32_t qt = rv + 2 * 64 * BV * 2;           // per parity: q~ image (64 x K)
   // per parity: [k~ (64 x 128 MN-major, A of MMA2) | Gamma_last (K fp32)]
   static constexpr uint32_t kb = qt + 2 * 128 * K;
   static constexpr uint32_t kb_gam = 2 * kPanel64;
@@ -77,11 +80,11 @@ struct RecLayout {
 // Tensor memory columns: D12 = [D1 | D2] of chunk parity b at b (K + 64). D2 accumulates the
 // chain's WQ S; once D1 is read, WQ (fp16 pairs, the A operand of MMA1) replaces its first
 // K / 2 columns. D3 follows both.
-template <int K>
+template <int K, int BV>
 struct RecTmem {
-  static constexpr uint32_t d12 = K + 64;
+  static constexpr uint32_t d12 = K + BV;
   static constexpr uint32_t d3 = 2 * d12;
-  static_assert(d3 + 64 <= 512, "tensor memory columns");
+  static_assert(d3 + BV <= 512, "tensor memory columns");
 };
 
 // Small per-CTA state after the operand buffers. Arrays of two are per chunk parity.
@@ -96,11 +99,12 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-template <int K>
+template <int K, int BV>
 __global__ void __launch_bounds__(kRecThreads, 1)
 recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
-  using Lay = RecLayout<K>;
-  using Tm = RecTmem<K>;
+  using Lay = RecLayout<K, BV>;
+  using Tm = RecTmem<K, BV>;
+  constexpr int CW = BV >= 32 ? 32 : 16;   // TMEM columns read per wait in the chain
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // 1024-byte aligned base, derived from the __shared__ array by pointer arithmetic so that the
   // compiler keeps every access in the shared address space
@@ -108,11 +112,11 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   RecMisc &ms = *reinterpret_cast<RecMisc *>(sm + Lay::misc);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int VT = p.V / kBV;
+  const int VT = p.V / BV;
   const int bid = blockIdx.x;
   const int r = bid / (p.H * VT);
   const int h = (bid / VT) % p.H;
-  const int v0 = (bid % VT) * kBV;
+  const int v0 = (bid % VT) * BV;
   if (p.flag && *p.flag != kDevOk) return;
   const int s = p.cu ? p.order[r] : r;
   const SeqInfo si = seq_info(p, s);
@@ -144,14 +148,14 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
     umma::mbar_fence_init();
     ms.err = 0;
   }
-  // chain threads: state master S[k][0:64] (fp32, thread k) and its fp16 operand copy
-  float S[kBV];
+  // chain threads: state master S[k][0:BV] (fp32, thread k) and its fp16 operand copy
+  float S[BV];
   if (is_chain && tid < K) {
 #pragma unroll
-    for (int v = 0; v < kBV; ++v)
+    for (int v = 0; v < BV; ++v)
       S[v] = p.init ? p.init[(((long long)s * p.H + h) * p.V + v0 + v) * K + tid] : 0.f;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < BV / 8; ++c) {
       uint4 w;
       w.x = pack_half2(S[8 * c + 0], S[8 * c + 1]);
       w.y = pack_half2(S[8 * c + 2], S[8 * c + 3]);
@@ -172,9 +176,9 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   auto stage_in = [&](int n) {
     const int b = n & 1;
     static_assert(Lay::mk_kg == hand_off_kg(K), "input buffer layout");
-    umma::mbar_arrive_expect_tx(&ms.bar_in[b], (uint32_t)(hand_off_qt(K) + kChunk * kBV * 2));
+    umma::mbar_arrive_expect_tx(&ms.bar_in[b], (uint32_t)(hand_off_qt(K) + kChunk * BV * 2));
     umma::bulk_g2s(sm + Lay::mk + b * Lay::mk_size, slot_of(n), (uint32_t)hand_off_qt(K), &ms.bar_in[b]);
-    umma::tma_load_4d(sm + Lay::rv + b * (kChunk * kBV * 2), &maps.v, v0, h, si.t0 + n * kChunk, si.b, &ms.bar_in[b]);
+    umma::tma_load_4d(sm + Lay::rv + b * (kChunk * BV * 2), &maps.v, v0, h, si.t0 + n * kChunk, si.b, &ms.bar_in[b]);
   };
   auto stage_qt = [&](int n) {
     const int b = n & 1;
@@ -233,7 +237,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       wait_bar(&ms.bar_wq[b], ph);
       const float gam = (tid < K) ? reinterpret_cast<const float *>(kb + Lay::kb_gam)[tid] : 0.f;
       if (tid == 0 && !bad) {   // D2 += WQ S  ->  [-U ; O]; WQ (A operand) in tensor memory
-        const uint32_t id = umma::idesc_f16(128, kBV, 0, 1);
+        const uint32_t id = umma::idesc_f16(128, BV, 0, 1);
         const uint64_t b0 = umma::sdesc_sw128(sbase + Lay::Sh, K * 128, 1024);
 #pragma unroll
         for (int ks = 0; ks < K / 16; ++ks) umma::mma_f16_ts(tD2, tD12 + ks * 8, umma::desc_add(b0, ks * 2048), id, 1);
@@ -242,13 +246,14 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       wait_bar(&ms.bar_mma1, (uint32_t)(n & 1));
       // U (rows < 64) -> fp16 operand; o = scale * O (rows >= 64) -> bf16 global
 #pragma unroll 1
-      for (int c0 = 0; c0 < kBV; c0 += 32) {
-        float x[32];
-        umma::tmem_ld32(tD2 + lane_base + c0, x);
+      for (int c0 = 0; c0 < BV; c0 += CW) {
+        float x[CW];
+        if constexpr (CW == 32) umma::tmem_ld32(tD2 + lane_base + c0, x);
+        else umma::tmem_ld16(tD2 + lane_base + c0, x);
         umma::tmem_ld_wait();
         if (tid < kChunk) {
 #pragma unroll
-          for (int hc = 0; hc < 4; ++hc) {
+          for (int hc = 0; hc < CW / 8; ++hc) {
             uint4 w;
             w.x = pack_half2(-x[8 * hc + 0], -x[8 * hc + 1]);
             w.y = pack_half2(-x[8 * hc + 2], -x[8 * hc + 3]);
@@ -259,7 +264,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
         } else if (tid - kChunk < L && !bad) {
           uint4 *dst = reinterpret_cast<uint4 *>(p.o + tok_row(p, si.b, t0 + tid - kChunk, h) * p.V + v0 + c0);
 #pragma unroll
-          for (int hc = 0; hc < 4; ++hc) {
+          for (int hc = 0; hc < CW / 8; ++hc) {
             __nv_bfloat16 ob[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) ob[j] = __float2bfloat16_rn(p.scale * x[8 * hc + j]);
@@ -272,7 +277,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       umma::named_bar(kBarChain, kChainThreads);
       if (tid == 0 && !bad) {   // D3 = k~^T U
         umma::fence_after_sync();
-        const uint32_t id = umma::idesc_f16(128, kBV, 1, 1);
+        const uint32_t id = umma::idesc_f16(128, BV, 1, 1);
         const uint64_t a0 = umma::sdesc_sw128(sbase + Lay::kb + b * Lay::kb_size, Lay::kPanel64, 1024);
         const uint64_t b0 = umma::sdesc_sw128(sbase + Lay::Uh, Lay::kPanel64, 1024);
 #pragma unroll
@@ -284,14 +289,15 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       // S = gamma S + D3 (thread = channel), fp16 copy for the next chunk
       if (tid < K) {
 #pragma unroll
-        for (int c0 = 0; c0 < kBV; c0 += 32) {
-          float x[32];
-          umma::tmem_ld32(tD3 + lane_base + c0, x);
+        for (int c0 = 0; c0 < BV; c0 += CW) {
+          float x[CW];
+          if constexpr (CW == 32) umma::tmem_ld32(tD3 + lane_base + c0, x);
+          else umma::tmem_ld16(tD3 + lane_base + c0, x);
           umma::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) S[c0 + j] = fmaf(gam, S[c0 + j], x[j]);
+          for (int j = 0; j < CW; ++j) S[c0 + j] = fmaf(gam, S[c0 + j], x[j]);
 #pragma unroll
-          for (int hc = 0; hc < 4; ++hc) {
+          for (int hc = 0; hc < CW / 8; ++hc) {
             uint4 w;
             const float *sv = &S[c0 + 8 * hc];
             w.x = pack_half2(sv[0], sv[1]);
@@ -312,7 +318,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
     const int b = sg;
     const uint32_t tD12 = tmem + Tm::d12 * b;
     unsigned char *mkb = sm + Lay::mk + b * Lay::mk_size;
-    __nv_bfloat16 *rvb = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::rv + b * (kChunk * kBV * 2));
+    __nv_bfloat16 *rvb = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::rv + b * (kChunk * BV * 2));
     const unsigned char *qtb = sm + Lay::qt + b * (128 * K);
     const int row = (warp & 3) * 32 + lane;   // TMEM lane of this warp's quadrant
     for (int n = sg; n < nch; n += 2) {
@@ -322,17 +328,17 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       wait_bar(&ms.bar_in[b], ph);
       in_done += bad ? 0u : 1u;
       if (L < kChunk) {   // v rows past the sequence end (next packed sequence or zero fill): zero them
-        for (int x = lt; x < (kChunk - L) * (kBV / 8); x += kSubThreads) {
-          const int i = L + x / (kBV / 8), c8 = x % (kBV / 8);
-          *reinterpret_cast<uint4 *>(rvb + i * kBV + 8 * c8) = make_uint4(0, 0, 0, 0);
+        for (int x = lt; x < (kChunk - L) * (BV / 8); x += kSubThreads) {
+          const int i = L + x / (BV / 8), c8 = x % (BV / 8);
+          *reinterpret_cast<uint4 *>(rvb + i * BV + 8 * c8) = make_uint4(0, 0, 0, 0);
         }
         umma::named_bar(sub_bar(sg), kSubThreads);
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < kChunk * BV / 8 / kSubThreads; ++j) {   // 16-byte chunks of the tile
         const int x = lt + kSubThreads * j;
-        const int i = x >> 3, cc = x & 7;
-        const uint4 raw = *reinterpret_cast<const uint4 *>(rvb + i * kBV + 8 * cc);
+        const int i = x / (BV / 8), cc = x % (BV / 8);
+        const uint4 raw = *reinterpret_cast<const uint4 *>(rvb + i * BV + 8 * cc);
         const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
         const float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]);
         const float2 f2 = __bfloat1622float2(b2[2]), f3 = __bfloat1622float2(b2[3]);
@@ -351,7 +357,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       if (lt == 0 && !bad) {
         if (n >= 2) stage_kt(n);
         umma::fence_after_sync();
-        const uint32_t id = umma::idesc_f16(128, K + kBV, 0, 1);   // D12 = M [khat Gamma | v]
+        const uint32_t id = umma::idesc_f16(128, K + BV, 0, 1);   // D12 = M [khat Gamma | v]
         const uint64_t a0 = umma::sdesc_sw128(umma::smem_u32(mkb), 16, 1024);
         const uint64_t b0 = umma::sdesc_sw128(umma::smem_u32(mkb + Lay::mk_kg), Lay::kPanel64, 1024);
 #pragma unroll
@@ -428,26 +434,39 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
     if (tid == 0) atomicExch(p.dev_status, kDevWaitTimeout);
   } else if (is_chain && p.final_state && tid < K) {
 #pragma unroll
-    for (int v = 0; v < kBV; ++v) p.final_state[(((long long)s * p.H + h) * p.V + v0 + v) * K + tid] = S[v];
+    for (int v = 0; v < BV; ++v) p.final_state[(((long long)s * p.H + h) * p.V + v0 + v) * K + tid] = S[v];
   }
   if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int K>
+template <int K, int BV>
 static cudaError_t launch_recur_t(const Problem &p, const TmaMaps &maps, cudaStream_t stream) {
-  const size_t smem = RecLayout<K>::bytes;
+  const size_t smem = RecLayout<K, BV>::bytes;
   static_assert(sizeof(RecMisc) <= 1024, "misc block");
-  cudaError_t e = cudaFuncSetAttribute(recur_tc_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(recur_tc_kernel<K, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)p.N * p.H * (p.V / kBV);
-  recur_tc_kernel<K><<<(unsigned)grid, kRecThreads, smem, stream>>>(p, maps);
+  const long long grid = (long long)p.N * p.H * (p.V / BV);
+  recur_tc_kernel<K, BV><<<(unsigned)grid, kRecThreads, smem, stream>>>(p, maps);
   return cudaGetLastError();
 }
 
-cudaError_t launch_recur(const Problem &p, const TmaMaps &maps, cudaStream_t stream) {
+// V-slice width: 64 unless that leaves fewer than about 80% of the SMs with a CTA.
+int recur_slice_width(const Problem &p) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return kBVWide;
+  }
+  const long long wide_ctas = (long long)p.N * p.H * (p.V / kBVWide);
+  return (5 * wide_ctas >= 4LL * sms) ? kBVWide : kBVNarrow;
+}
+
+cudaError_t launch_recur(const Problem &p, const TmaMaps &maps, int bv, cudaStream_t stream) {
   if (p.N == 0) return cudaSuccess;
-  return p.K == 64 ? launch_recur_t<64>(p, maps, stream) : launch_recur_t<128>(p, maps, stream);
+  if (bv == kBVNarrow)
+    return p.K == 64 ? launch_recur_t<64, kBVNarrow>(p, maps, stream) : launch_recur_t<128, kBVNarrow>(p, maps, stream);
+  return p.K == 64 ? launch_recur_t<64, kBVWide>(p, maps, stream) : launch_recur_t<128, kBVWide>(p, maps, stream);
 }
 
 }  // namespace kda

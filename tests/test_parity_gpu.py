@@ -18,12 +18,15 @@ def test_tiny_config():
 
 # Shapes of the reference's end-to-end KDA tests (B-T-H-D: 1-63-1-128, 2-500-3-128,
 # 2-1000-3-128, 3-1024-4-128, ...: T need not be a multiple of the chunk) plus
-# head dim 64 and the chunk edges T = 1, 64, 65.
+# head dim 64 and the chunk edges T = 1, 64, 65. The recurrence kernel takes 16-column V slices
+# when 64-column slices would leave most SMs idle: the small shapes run that way, the last two
+# (128 sequence-head pairs x 64-column slices) run with 64-column slices.
 SHAPES = [
     (1, 63, 1, 128, 128, -5.0, True), (2, 500, 3, 128, 128, -5.0, False), (2, 1000, 3, 128, 128, -1.0, True),
     (3, 1024, 4, 128, 128, -5.0, True), (1, 1, 2, 64, 64, -5.0, True), (1, 64, 2, 64, 64, -0.1, True),
     (1, 65, 2, 64, 64, -5.0, False), (2, 130, 2, 64, 64, -2.0, True), (1, 200, 2, 64, 128, -5.0, True),
     (1, 200, 2, 128, 64, -0.5, True), (1, 333, 2, 128, 128, 0.0, True),
+    (4, 200, 32, 64, 64, -5.0, True), (2, 130, 32, 128, 128, -3.0, True),
 ]
 
 
