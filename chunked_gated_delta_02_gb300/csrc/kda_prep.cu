@@ -148,29 +148,6 @@ prep_kernel(const Problem p) {
   const int len = min(kChunk, si.len - n * kChunk);
   const uint32_t sbase = umma::smem_u32(sm);
 
-  // ---- pass 0: beta sigmoid, TMEM, barrier
-  if (tid < kChunk)
-    ms.beta[tid] = (tid < len) ? sigmoid_fast(__bfloat162float(p.beta[tok_row(p, si.b, t0 + tid, h)])) : 0.f;
-  if (warp == 0) {
-    umma::tmem_alloc(&ms.tmem_slot, kPrepTmemCols);
-    umma::tmem_relinquish();
-  }
-  if (tid == 32) {
-    umma::mbar_init(&ms.bar, 1);
-    umma::mbar_fence_init();
-    ms.err = 0;
-  }
-  umma::fence_before_sync();
-  __syncthreads();
-  umma::fence_after_sync();
-  const uint32_t tmem = ms.tmem_slot;
-  uint32_t waits = 0;   // completed waits on ms.bar (its phase parity)
-  auto wait_mma = [&]() {
-    if (!umma::mbar_wait_bounded(&ms.bar, waits & 1, kPrepWaitLimit)) atomicExch(&ms.err, 1);
-    ++waits;
-    umma::fence_after_sync();
-  };
-
   // Elementwise unit of this thread: channel quad cq = lane % 16 of the current half (channels
   // 4 cq .. 4 cq + 3) and the 4-row sub-block sb4 = 2 warp + lane / 16 (rows 4 sb4 .. + 3), which
   // is sub-block sbi = sb4 % 4 of the 16-row block J = sb4 / 4. A warp covers two rows of 64
@@ -178,8 +155,6 @@ prep_kernel(const Problem p) {
   const int cq = lane & 15, sb4 = 2 * warp + (lane >> 4), J = sb4 >> 2, sbi = sb4 & 3;
   const int row0 = 4 * sb4;
   const int nrows = max(0, min(4, len - row0));
-  const float ea = expf(p.A_log[h]);
-  const float cg = -ea * kLog2e;                 // sigmoid(a) = 1 / (1 + 2^{cg (g + dt)})
   const float lbl2 = p.lb * kLog2e;
   const long long rstride = (long long)p.H * K;  // elements between consecutive tokens
   const long long rbase = tok_row(p, si.b, t0 + row0, h) * K;
@@ -206,26 +181,56 @@ prep_kernel(const Problem p) {
   for (int r = 0; r < 4; ++r) roff[r] = rbase + (long long)min(r, max(nrows - 1, 0)) * rstride;
   auto row_off = [&](int r) -> long long { return roff[r]; };
 
-  // ---- pass 1: row norms |k_i|, |q_i| over all channels (this thread's 4 rows); g goes to L2 meanwhile
+  // The global loads of the norm pass (k and q of this thread's rows, both halves) and beta are
+  // issued before the setup below, so that their latency overlaps it.
+  uint2 rk[K / 64][4], rq[K / 64][4];
+  if (nrows > 0) {
+#pragma unroll
+    for (int hf = 0; hf < K / 64; ++hf) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const long long off = row_off(r) + 64 * hf + 4 * cq;
+        rk[hf][r] = ldg_u64(p.k + off);
+        rq[hf][r] = ldg_u64(p.q + off);
+      }
+    }
+    if (cq < 4 * (K / 64)) {   // g of the sub-block to L2: one prefetch per (row, 128-byte line)
+      const int r = cq / (K / 64), line = cq % (K / 64);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.g + rbase + (long long)min(r, nrows - 1) * rstride + 64 * line));
+    }
+  }
+  __nv_bfloat16 beta_raw = __float2bfloat16(0.f);   // beta logit of token tid (tid < 64)
+  if (tid < len) beta_raw = p.beta[tok_row(p, si.b, t0 + tid, h)];
+  const float a_log = p.A_log[h];
+
+  // ---- pass 0: TMEM, barrier
+  if (warp == 0) {
+    umma::tmem_alloc(&ms.tmem_slot, kPrepTmemCols);
+    umma::tmem_relinquish();
+  }
+  if (tid == 32) {
+    umma::mbar_init(&ms.bar, 1);
+    umma::mbar_fence_init();
+    ms.err = 0;
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = ms.tmem_slot;
+  const float cg = -expf(a_log) * kLog2e;   // sigmoid(a) = 1 / (1 + 2^{cg (g + dt)})
+  uint32_t waits = 0;   // completed waits on ms.bar (its phase parity)
+  auto wait_mma = [&]() {
+    if (!umma::mbar_wait_bounded(&ms.bar, waits & 1, kPrepWaitLimit)) atomicExch(&ms.err, 1);
+    ++waits;
+    umma::fence_after_sync();
+  };
+
+  // ---- pass 1: row norms |k_i|, |q_i| over all channels (this thread's 4 rows)
   {
     float red[8];   // per row: |k|^2 (0..3) and |q|^2 (4..7) over this lane's channel quads
 #pragma unroll
     for (int r = 0; r < 8; ++r) red[r] = 0.f;
     if (nrows > 0) {
-      uint2 rk[K / 64][4], rq[K / 64][4];
-#pragma unroll
-      for (int hf = 0; hf < K / 64; ++hf) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const long long off = row_off(r) + 64 * hf + 4 * cq;
-          rk[hf][r] = ldg_u64(p.k + off);
-          rq[hf][r] = ldg_u64(p.q + off);
-        }
-      }
-      if (cq < 4 * (K / 64)) {   // g of the sub-block to L2: one prefetch per (row, 128-byte line)
-        const int r = cq / (K / 64), line = cq % (K / 64);
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.g + rbase + (long long)min(r, nrows - 1) * rstride + 64 * line));
-      }
 #pragma unroll
       for (int hf = 0; hf < K / 64; ++hf) {
 #pragma unroll
@@ -269,7 +274,7 @@ prep_kernel(const Problem p) {
 
 #pragma unroll 1
   for (int hf = 0; hf < K / 64; ++hf) {
-    // ---- pass 2a: gate and log decay of 4 rows x 4 channels
+    // ---- pass 2a: gate and log decay of 4 rows x 4 channels (k and q as loaded by pass 1)
     const int kk = 64 * hf + 4 * cq;
     uint2 rawk[4], rawq[4], rawg[4];
 #pragma unroll
@@ -277,10 +282,9 @@ prep_kernel(const Problem p) {
     if (nrows > 0) {   // no load at all when the whole sub-block is past the sequence end
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const long long off = row_off(r) + kk;
-        rawg[r] = ldg_u64(p.g + off);
-        rawk[r] = ldg_u64(p.k + off);
-        rawq[r] = ldg_u64(p.q + off);
+        rawg[r] = ldg_u64(p.g + row_off(r) + kk);
+        rawk[r] = (K == 128 && hf > 0) ? rk[K / 64 - 1][r] : rk[0][r];
+        rawq[r] = (K == 128 && hf > 0) ? rq[K / 64 - 1][r] : rq[0][r];
       }
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
@@ -305,6 +309,7 @@ prep_kernel(const Problem p) {
       qv[r] = bf4_to_f4(rawq[r]);
     }
     ms.ssub[J][sbi][cq] = float4_of(ssum);
+    if (hf == 0 && tid < kChunk) ms.beta[tid] = (tid < len) ? sigmoid_fast(__bfloat162float(beta_raw)) : 0.f;
     __syncthreads();
 
     // ---- pass 2b: operands of the A/P product for this half (tf32, rounded to nearest), and the
@@ -432,45 +437,45 @@ prep_kernel(const Problem p) {
       }
     }
   }
-  // the -I half of [-I ; P], and zeros above the block diagonal of P and T, as 16-byte stores of
-  // (row i, 4-column group cq); A above its block diagonal is never read
-#pragma unroll 1
-  for (int x = tid; x < 64 * 16; x += kPrepThreads) {
-    const int i = x >> 4, cq = x & 15;
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    const bool dg = (i >> 2) == cq;   // this group holds the diagonal entry (i, i)
-    const float4 v = make_float4(dg && (i & 3) == 0 ? -1.f : 0.f, dg && (i & 3) == 1 ? -1.f : 0.f,
-                                 dg && (i & 3) == 2 ? -1.f : 0.f, dg && (i & 3) == 3 ? -1.f : 0.f);
-    unsigned char *pan = sm + Lay::opM + (uint32_t)(cq >> 3) * (128 * 128);
-    *reinterpret_cast<float4 *>(pan + umma::sw128_chunk(i, cq & 7)) = v;
-    if (cq >= 4 * ((i >> 4) + 1)) {
-      *reinterpret_cast<float4 *>(pan + umma::sw128_chunk(64 + i, cq & 7)) = z;
-      *reinterpret_cast<float4 *>(&matT[i][4 * cq]) = z;
+  if (tid < 64) {
+    // ---- pass 4a (warps 0-1): diagonal blocks of T by forward substitution. Thread = column col
+    // of diagonal block Jd, its 16 rows in registers: x_i = [i == col] - sum_{j < i} A_ij x_j, the
+    // terms in order of j so that x_{i-1} enters last. The 16 threads of a block read the same
+    // A rows (broadcast 16-byte loads).
+    const int Jd = tid >> 4, col = tid & 15, o = 16 * Jd;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float acc = (i == col) ? 1.f : 0.f;
+#pragma unroll
+      for (int q = 0; q < (i + 3) / 4; ++q) {
+        const float4 a = *reinterpret_cast<const float4 *>(&matA[o + i][o + 4 * q]);
+        acc = fmaf(-a.x, x[4 * q], acc);
+        if (4 * q + 1 < i) acc = fmaf(-a.y, x[4 * q + 1], acc);
+        if (4 * q + 2 < i) acc = fmaf(-a.z, x[4 * q + 2], acc);
+        if (4 * q + 3 < i) acc = fmaf(-a.w, x[4 * q + 3], acc);
+      }
+      x[i] = acc;
     }
-  }
-  __syncthreads();
-
-  // ---- pass 4a: diagonal blocks of T by forward substitution. Thread = (column of a diagonal
-  // block, quarter of its rows): column c = tid / 4 of block Jd = c / 16, rows 4 qr .. 4 qr + 3 of
-  // the block in registers. At step j the thread holding row j shares it with its column's
-  // other three threads (one shuffle), which update their rows below j.
-  {
-    const int cix = tid >> 2, qr = tid & 3;
-    const int Jd = cix >> 4, col = cix & 15, o = 16 * Jd;
-    float x[4];
 #pragma unroll
-    for (int s2 = 0; s2 < 4; ++s2) x[s2] = (4 * qr + s2 == col) ? 1.f : 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float xj = __shfl_sync(0xffffffffu, x[j & 3], (lane & ~3) | (j >> 2));
-#pragma unroll
-      for (int s2 = 0; s2 < 4; ++s2) {
-        const int i = 4 * qr + s2;
-        if (i > j) x[s2] = fmaf(-matA[o + i][o + j], xj, x[s2]);
+    for (int i = 0; i < 16; ++i) matT[o + i][o + col] = x[i];
+  } else {
+    // warps 2-7 meanwhile: the -I half of [-I ; P], and zeros above the block diagonal of P and T,
+    // as 16-byte stores of (row i, 4-column group cq); A above its block diagonal is never read
+#pragma unroll 1
+    for (int x = tid - 64; x < 64 * 16; x += kPrepThreads - 64) {
+      const int i = x >> 4, cq = x & 15;
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      const bool dg = (i >> 2) == cq;   // this group holds the diagonal entry (i, i)
+      const float4 v = make_float4(dg && (i & 3) == 0 ? -1.f : 0.f, dg && (i & 3) == 1 ? -1.f : 0.f,
+                                   dg && (i & 3) == 2 ? -1.f : 0.f, dg && (i & 3) == 3 ? -1.f : 0.f);
+      unsigned char *pan = sm + Lay::opM + (uint32_t)(cq >> 3) * (128 * 128);
+      *reinterpret_cast<float4 *>(pan + umma::sw128_chunk(i, cq & 7)) = v;
+      if (cq >= 4 * ((i >> 4) + 1)) {
+        *reinterpret_cast<float4 *>(pan + umma::sw128_chunk(64 + i, cq & 7)) = z;
+        *reinterpret_cast<float4 *>(&matT[i][4 * cq]) = z;
       }
     }
-#pragma unroll
-    for (int s2 = 0; s2 < 4; ++s2) matT[o + 4 * qr + s2][o + col] = x[s2];
   }
   __syncthreads();
   // ---- pass 4b: off-diagonal blocks of T by doubling (four steps). A thread computes a strip of
