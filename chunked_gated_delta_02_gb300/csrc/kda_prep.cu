@@ -10,11 +10,12 @@
 //   * M = [ -Tb ; P Tb ] (128 x 64 fp16, rows in 128-byte-swizzled order),
 //       Tb = (I + A)^{-1} diag(beta)
 //       A_ij = beta_i sum_k khat_ik khat_jk 2^{G_ik - G_jk}   (j < i)
-//       P_ij =        sum_k qhat_ik khat_jk 2^{G_ik - G_jk}   (j <= i)
-//   * khat Gamma, khat Gamma_last / Gamma and qhat Gamma (64 x K fp16 each, as
+//       P_ij = scale  sum_k qhat_ik khat_jk 2^{G_ik - G_jk}   (j <= i)
+//   * khat Gamma, khat Gamma_last / Gamma and scale qhat Gamma (64 x K fp16 each, as
 //     images of 64-channel panels of 128-byte swizzled token rows) and
 //     Gamma_last (K fp32),
-// with G the in-chunk inclusive cumulative base-2 log decay and Gamma = 2^G.
+// with G the in-chunk inclusive cumulative base-2 log decay and Gamma = 2^G. The output
+// scale sits in P and in the q image, so the recurrence kernel's O rows come out scaled.
 // With these the recurrence kernel forms w = Tb (khat Gamma), u = Tb v, P w and
 // P u as plain products. The log decay per token and channel is
 // la2 = lb log2(e) sigmoid(exp(A_log)(g + dt_bias)).
@@ -45,11 +46,11 @@
 //   D = [k X ; q X] (128 x K)  x  [k Y ; k Ys ; k Ys_0 2^{B_1} ; k Ys_1 2^{B_2} ; k Ys_0 c_30]^T
 // Columns 0-63 give the diagonal blocks, 64-127 the blocks next to the
 // diagonal, 128-175 the three blocks further out. The unit lower triangular
-// inverse T = (I + A)^{-1} is blocked: the four 16 x 16 diagonal blocks by
-// forward substitution (one thread per column), then the off-diagonal blocks by
-// doubling, in fp32: the 32 x 32 halves T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22,
-// then the lower-left 32 x 32 block -T_[23] A_[23][01] T_[01]. Finally
-// M = [-I ; P] Tb is a second tensor-core product (128 x 64 x 64).
+// inverse T = (I + A)^{-1} is blocked, in fp32: the two 32 x 32 diagonal halves by
+// forward substitution (one thread per column), then the lower-left 32 x 32 block
+// -T_[23] A_[23][01] T_[01] as 16 x 16 block products. Both write Tb = T diag(beta)
+// straight into the operand of M = [-I ; P] Tb, a second tensor-core product
+// (128 x 64 x 64).
 #include "kda_common.cuh"
 #include "umma.cuh"
 
@@ -66,11 +67,15 @@ struct PrepLayout {
   static constexpr uint32_t opA = 0;                            // [k X ; q X]: 2 panels x 128 rows x 128 B
   static constexpr uint32_t opB = opA + 2 * 128 * 128;          // J side:      2 panels x 176 rows x 128 B
   static constexpr uint32_t opEnd = opB + 2 * kOpBRows * 128;
-  // after the A/P product the operands are dead: A and T (fp32 [64][68]), the merge scratch,
-  // the Tb^T operand and the [-I ; P] operand take their place
+  // after the A/P product the operands are dead: A (its lower-left quarter [32][36] row-major and
+  // its two diagonal halves transposed, [2 x 32][36]), T (fp32 [64][68]), the merge scratch, the
+  // Tb^T operand and the [-I ; P] operand take their place
   static constexpr int LD = 68;                                 // 68 = 4 (mod 32) words: conflict-free rows
-  static constexpr uint32_t matA = 0;
-  static constexpr uint32_t matT = matA + 64 * LD * 4;
+  static constexpr int LDQ = 36;                                // 16-byte aligned rows of 32 + 4
+  static constexpr uint32_t matAll = 0;
+  static constexpr uint32_t matAt = matAll + 32 * LDQ * 4;
+  static constexpr uint32_t matT = 64 * LD * 4;
+  static_assert(matAt + 64 * LDQ * 4 <= matT, "A overlaps T");
   static constexpr uint32_t Z = matT + 64 * LD * 4;             // [4][16][16] fp32 merge scratch
   static constexpr uint32_t opT = 38 * 1024;                    // Tb^T:     2 panels x  64 rows x 128 B
   static constexpr uint32_t opM = 54 * 1024;                    // [-I ; P]: 2 panels x 128 rows x 128 B
@@ -131,7 +136,8 @@ prep_kernel(const Problem p) {
   // compiler keeps every access in the shared address space
   unsigned char *sm = smem_raw + ((1024u - (umma::smem_u32(smem_raw) & 1023u)) & 1023u);
   PrepMisc &ms = *reinterpret_cast<PrepMisc *>(sm + Lay::end);
-  float (*matA)[Lay::LD] = reinterpret_cast<float (*)[Lay::LD]>(sm + Lay::matA);
+  float (*matAll)[Lay::LDQ] = reinterpret_cast<float (*)[Lay::LDQ]>(sm + Lay::matAll);   // A[32 + r][c]
+  float (*matAt)[Lay::LDQ] = reinterpret_cast<float (*)[Lay::LDQ]>(sm + Lay::matAt);     // A[32 h + c][32 h + r] at [32 h + r][c]
   float (*matT)[Lay::LD] = reinterpret_cast<float (*)[Lay::LD]>(sm + Lay::matT);
   float (*Zs)[16][16] = reinterpret_cast<float (*)[16][16]>(sm + Lay::Z);   // [4][16][16]
 
@@ -356,7 +362,7 @@ prep_kernel(const Problem p) {
       const F4 G = mul4(X, PJ);
       const uint32_t io = img_off(r);
       st_half4(kg_img + io, mul4(kv[r], mul4(G, splat4(ms.kn[i]))));
-      st_half4(qt_img + io, mul4(qv[r], mul4(G, splat4(ms.qn[i]))));
+      st_half4(qt_img + io, mul4(qv[r], mul4(G, splat4(ms.qn[i] * p.scale))));
     }
 #pragma unroll
     for (int r = 3; r >= 0; --r) {  // J side; Gamma_last / Gamma = Ys 2^{blocks after J}
@@ -390,13 +396,14 @@ prep_kernel(const Problem p) {
   // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (lane = D row). A lane quadrant holds the row
   // blocks {0, 1} (quadrants 0, 2) or {2, 3} (quadrants 1, 3), which need the 16-column blocks
   // {0, 1, 4} or {2, 3, 5, 6, 8, 9, 10}; the two warps of a quadrant split them and load all of
-  // theirs before one wait. A rows (< 64) go to fp32 matA (times beta_i |k_i|^-1 |k_j|^-1,
-  // strictly lower), P rows to the [-I ; P] operand (times |q_i|^-1 |k_j|^-1, lower with the
+  // theirs before one wait. A rows (< 64) go to fp32 matAt (blocks of the diagonal halves,
+  // transposed) or matAll (the lower-left quarter), times beta_i |k_i|^-1 |k_j|^-1, strictly
+  // lower; P rows to the [-I ; P] operand (times |q_i|^-1 |k_j|^-1, lower with the
   // diagonal, tf32).
   {
     const int row = 32 * (warp & 3) + lane, I = (row & 63) >> 4;
     const bool isA = row < 64;
-    const float rowf = isA ? ms.beta[row] * ms.kn[row] : ms.qn[row - 64];
+    const float rowf = isA ? ms.beta[row] * ms.kn[row] : ms.qn[row - 64] * p.scale;
     const int thr = isA ? row : row - 63;   // column j is kept when j < thr
     const int xs = isA ? 0 : (row & 7);
     const int sel = (warp & 1) * 2 + (warp >> 2);   // (upper row blocks, second warp of the quadrant)
@@ -419,7 +426,20 @@ prep_kernel(const Problem p) {
       else if (cb == 8) Jb = (I == 2) ? 0 : -1;
       else Jb = (I == 3) ? (cb == 9 ? 1 : 0) : -1;
       if (Jb < 0) continue;
-      unsigned char *rowp = isA ? reinterpret_cast<unsigned char *>(&matA[row][0])
+      if (isA && (I >> 1) == (Jb >> 1)) {   // block of a diagonal half of A: transposed, scalar stores
+        float *atc = &matAt[32 * (Jb >> 1) + 16 * (Jb & 1)][row & 31];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 knj = *reinterpret_cast<const float4 *>(&ms.kn[16 * Jb + 4 * q]);
+          const float kj[4] = {knj.x, knj.y, knj.z, knj.w};
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2)
+            atc[(4 * q + e2) * Lay::LDQ] = (16 * Jb + 4 * q + e2 < thr) ? x[4 * q + e2] * rowf * kj[e2] : 0.f;
+        }
+        continue;
+      }
+      // lower-left quarter of A (rows >= 32, columns < 32), or a P row of the [-I ; P] operand
+      unsigned char *rowp = isA ? reinterpret_cast<unsigned char *>(&matAll[row - 32][0])
                                 : sm + Lay::opM + (uint32_t)(Jb >> 1) * (128 * 128) + (uint32_t)row * 128;
       const int c0 = isA ? 4 * Jb : 4 * (Jb & 1);
 #pragma unroll
@@ -437,49 +457,66 @@ prep_kernel(const Problem p) {
       }
     }
   }
+  // Tb^T operand (row j, column m: T[m][j] beta_j, tf32) in 2 panels of 32 columns m: the 16-byte
+  // chunk of (row j, columns m4 .. m4 + 3)
+  auto opT_chunk = [&](int j, int m4) -> unsigned char * {
+    return sm + Lay::opT + (uint32_t)(m4 >> 5) * (64 * 128) + umma::sw128_chunk(j, (m4 & 31) >> 2);
+  };
   if (tid < 64) {
-    // ---- pass 4a (warps 0-1): diagonal blocks of T by forward substitution. Thread = column col
-    // of diagonal block Jd, its 16 rows in registers: x_i = [i == col] - sum_{j < i} A_ij x_j, the
-    // terms in order of j so that x_{i-1} enters last. The 16 threads of a block read the same
-    // A rows (broadcast 16-byte loads).
-    const int Jd = tid >> 4, col = tid & 15, o = 16 * Jd;
-    float x[16];
+    // ---- pass 4a (warps 0-1): the 32 x 32 diagonal halves of T by forward substitution. Thread =
+    // column col of half hh, its 32 rows in registers. Step j, with x_j final, subtracts
+    // A_ij x_j from every x_i below it: independent FMAs, column j of A read as broadcast 16-byte
+    // loads of the transposed half. The column goes to matT (read by the lower-left merge) and,
+    // times beta, to row o + col of the Tb^T operand.
+    const int hh = tid >> 5, col = tid & 31, o = 32 * hh;
+    float x[32];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float acc = (i == col) ? 1.f : 0.f;
+    for (int i = 0; i < 32; ++i) x[i] = (i == col) ? 1.f : 0.f;
 #pragma unroll
-      for (int q = 0; q < (i + 3) / 4; ++q) {
-        const float4 a = *reinterpret_cast<const float4 *>(&matA[o + i][o + 4 * q]);
-        acc = fmaf(-a.x, x[4 * q], acc);
-        if (4 * q + 1 < i) acc = fmaf(-a.y, x[4 * q + 1], acc);
-        if (4 * q + 2 < i) acc = fmaf(-a.z, x[4 * q + 2], acc);
-        if (4 * q + 3 < i) acc = fmaf(-a.w, x[4 * q + 3], acc);
+    for (int j = 0; j < 31; ++j) {
+      const float xj = x[j];
+#pragma unroll
+      for (int q = (j + 1) / 4; q < 8; ++q) {
+        const float4 a = *reinterpret_cast<const float4 *>(&matAt[o + j][4 * q]);
+        if (4 * q + 0 > j) x[4 * q + 0] = fmaf(-a.x, xj, x[4 * q + 0]);
+        if (4 * q + 1 > j) x[4 * q + 1] = fmaf(-a.y, xj, x[4 * q + 1]);
+        if (4 * q + 2 > j) x[4 * q + 2] = fmaf(-a.z, xj, x[4 * q + 2]);
+        if (4 * q + 3 > j) x[4 * q + 3] = fmaf(-a.w, xj, x[4 * q + 3]);
       }
-      x[i] = acc;
     }
+    const float bj = ms.beta[o + col];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) matT[o + i][o + col] = x[i];
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<float4 *>(opT_chunk(o + col, o + 4 * c)) =
+          make_float4(tf32_rn(x[4 * c] * bj), tf32_rn(x[4 * c + 1] * bj), tf32_rn(x[4 * c + 2] * bj), tf32_rn(x[4 * c + 3] * bj));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) matT[o + i][o + col] = x[i];
   } else {
-    // warps 2-7 meanwhile: the -I half of [-I ; P], and zeros above the block diagonal of P and T,
-    // as 16-byte stores of (row i, 4-column group cq); A above its block diagonal is never read
+    // warps 2-7 meanwhile, as 16-byte stores: the -I half of [-I ; P] and the zeros above the
+    // block diagonal of P (row i, 4-column group cq), then the zero upper-right quarter of Tb^T
+    // (rows j >= 32, columns m < 32). A above its block diagonal is never read.
 #pragma unroll 1
-    for (int x = tid - 64; x < 64 * 16; x += kPrepThreads - 64) {
-      const int i = x >> 4, cq = x & 15;
+    for (int x = tid - 64; x < 64 * 16 + 32 * 8; x += kPrepThreads - 64) {
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (x >= 64 * 16) {
+        const int y = x - 64 * 16;
+        *reinterpret_cast<float4 *>(opT_chunk(32 + (y >> 3), 4 * (y & 7))) = z;
+        continue;
+      }
+      const int i = x >> 4, cq = x & 15;
       const bool dg = (i >> 2) == cq;   // this group holds the diagonal entry (i, i)
       const float4 v = make_float4(dg && (i & 3) == 0 ? -1.f : 0.f, dg && (i & 3) == 1 ? -1.f : 0.f,
                                    dg && (i & 3) == 2 ? -1.f : 0.f, dg && (i & 3) == 3 ? -1.f : 0.f);
       unsigned char *pan = sm + Lay::opM + (uint32_t)(cq >> 3) * (128 * 128);
       *reinterpret_cast<float4 *>(pan + umma::sw128_chunk(i, cq & 7)) = v;
-      if (cq >= 4 * ((i >> 4) + 1)) {
-        *reinterpret_cast<float4 *>(pan + umma::sw128_chunk(64 + i, cq & 7)) = z;
-        *reinterpret_cast<float4 *>(&matT[i][4 * cq]) = z;
-      }
+      if (cq >= 4 * ((i >> 4) + 1)) *reinterpret_cast<float4 *>(pan + umma::sw128_chunk(64 + i, cq & 7)) = z;
     }
   }
   __syncthreads();
-  // ---- pass 4b: off-diagonal blocks of T by doubling (four steps). A thread computes a strip of
-  // four columns of one row of a 16 x 16 block with 16-byte loads of T and Z rows.
+  // ---- pass 4b: the lower-left 32 x 32 block of T, -T_[23] A_[23][01] T_[01], in 16 x 16 blocks
+  // (row blocks a = 2, 3; column blocks b = 0, 1): Z_ab = sum_{b <= c <= 1} A_ac T_cb, then
+  // T_ab = -sum_{2 <= c <= a} T_ac Z_cb, written times beta to the Tb^T operand. A thread computes
+  // a strip of four columns of one row of a 16 x 16 block with 16-byte loads of T and Z rows.
   auto fma4 = [](float a, const float4 b, float4 &acc) {
     acc.x = fmaf(a, b.x, acc.x);
     acc.y = fmaf(a, b.y, acc.y);
@@ -500,48 +537,26 @@ prep_kernel(const Problem p) {
   };
   {
     const int i = (tid >> 2) & 15, c4 = 4 * (tid & 3);
-    // level 1, blocks (I, I - 1) for I = 1, 3: Z = A_{I,I-1} T_{I-1,I-1}, then T_{I,I-1} = -T_II Z
-    const int p1 = tid >> 6, I1 = 2 * p1 + 1;   // threads 0..127
-    if (tid < 128) {
-      float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      strip(&matA[16 * I1 + i][16 * (I1 - 1)], &matT[16 * (I1 - 1)][16 * (I1 - 1) + c4], Lay::LD, z);
-      *reinterpret_cast<float4 *>(&Zs[p1][i][c4]) = z;
-    }
-    __syncthreads();
-    if (tid < 128) {
-      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-      strip(&matT[16 * I1 + i][16 * I1], &Zs[p1][0][c4], 16, t);
-      *reinterpret_cast<float4 *>(&matT[16 * I1 + i][16 * (I1 - 1) + c4]) = make_float4(-t.x, -t.y, -t.z, -t.w);
-    }
-    __syncthreads();
-    // level 2, the lower-left 32 x 32 block (row blocks a = 2, 3; column blocks b = 0, 1):
-    // Z_ab = sum_{b <= c <= 1} A_ac T_cb, then T_ab = -sum_{2 <= c <= a} T_ac Z_cb
     const int a = 2 + (tid >> 7), b = (tid >> 6) & 1;
     {
       float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c = b; c <= 1; ++c) strip(&matA[16 * a + i][16 * c], &matT[16 * c][16 * b + c4], Lay::LD, z);
+      for (int c = b; c <= 1; ++c) strip(&matAll[16 * (a - 2) + i][16 * c], &matT[16 * c][16 * b + c4], Lay::LD, z);
       *reinterpret_cast<float4 *>(&Zs[2 * (a - 2) + b][i][c4]) = z;
     }
     __syncthreads();
     {
       float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int c = 2; c <= a; ++c) strip(&matT[16 * a + i][16 * c], &Zs[2 * (c - 2) + b][0][c4], 16, t);
-      *reinterpret_cast<float4 *>(&matT[16 * a + i][16 * b + c4]) = make_float4(-t.x, -t.y, -t.z, -t.w);
+      // T[m][j] for m = 16 a + i and j = 16 b + c4 .. + 3: element m % 4 of chunk (row j, m)
+      const int m = 16 * a + i, j = 16 * b + c4;
+      const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        reinterpret_cast<float *>(opT_chunk(j + e, m & ~3))[m & 3] = tf32_rn(-tv[e] * ms.beta[j + e]);
     }
-    __syncthreads();
   }
 
-  // ---- pass 5: Tb^T operand (row j, column m: T[m][j] beta_j), then M = [-I ; P] Tb on the tensor cores
-  // thread = (row j of Tb^T, 4-column group m4): one 16-byte store per item
-#pragma unroll 1
-  for (int x = tid; x < 64 * 16; x += kPrepThreads) {
-    const int j = x & 63, m4 = 4 * (x >> 6);
-    const float bj = ms.beta[j];
-    const float4 v = make_float4(tf32_rn(matT[m4][j] * bj), tf32_rn(matT[m4 + 1][j] * bj),
-                                 tf32_rn(matT[m4 + 2][j] * bj), tf32_rn(matT[m4 + 3][j] * bj));
-    *reinterpret_cast<float4 *>(sm + Lay::opT + (uint32_t)(m4 >> 5) * (64 * 128) +
-                                umma::sw128_chunk(j, (m4 & 31) >> 2)) = v;
-  }
+  // ---- pass 5: M = [-I ; P] Tb on the tensor cores
   umma::fence_proxy_async_smem();
   umma::fence_before_sync();
   __syncthreads();

@@ -12,7 +12,7 @@
 //   D2 = M v                     = [-u ; P u]        (128 x 64, UMMA 128x64x64)
 //   WQ = [w ; q~ - P w],  q~ = qhat Gamma            (fp16 operand)
 //   D2 += WQ S                   = [-U ; O]          (UMMA 128x64xK)
-//   U -> fp16, o = scale O -> bf16
+//   U -> fp16, o = O -> bf16   (the output scale is folded into P and q~)
 //   D3 = k~^T U,  k~ = khat Gamma_last / Gamma       (UMMA 128x64x64)
 //   S  = Gamma_last S + D3                           (fp32 master in registers)
 //
@@ -52,8 +52,9 @@ constexpr int kRecThreads = kChainThreads + 2 * kSubThreads;
 constexpr int kBVWide = 64, kBVNarrow = 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clocks per wait
-// named barrier ids (0 is __syncthreads): the chain, and prep sub-groups 0 and 1
-constexpr int kBarChain = 1;
+// named barrier ids (0 is __syncthreads): the chain, prep sub-groups 0 and 1, and the end of
+// the chain's D2 reads (U rows written, O rows read)
+constexpr int kBarChain = 1, kBarE = 4;
 __device__ __forceinline__ int sub_bar(int sg) { return 2 + sg; }
 
 template <int K, int BV>
@@ -244,13 +245,20 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
         umma::commit(&ms.bar_mma1);
       }
       wait_bar(&ms.bar_mma1, (uint32_t)(n & 1));
-      // U (rows < 64) -> fp16 operand; o = scale * O (rows >= 64) -> bf16 global
+      // U (rows < 64) -> fp16 operand; o = O (rows >= 64, the scale is folded into P and q~) ->
+      // bf16 global. D3 = k~^T U needs U complete and, since its commit releases D2 to the next
+      // chunk of this parity, every D2 read done: the U warps wait at kBarE, the O warps only
+      // arrive there once their last read is complete and store o after.
 #pragma unroll 1
       for (int c0 = 0; c0 < BV; c0 += CW) {
         float x[CW];
         if constexpr (CW == 32) umma::tmem_ld32(tD2 + lane_base + c0, x);
         else umma::tmem_ld16(tD2 + lane_base + c0, x);
         umma::tmem_ld_wait();
+        if (tid >= kChunk && c0 + CW >= BV) {
+          umma::fence_before_sync();
+          umma::named_arrive(kBarE, kChainThreads);
+        }
         if (tid < kChunk) {
 #pragma unroll
           for (int hc = 0; hc < CW / 8; ++hc) {
@@ -267,14 +275,16 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
           for (int hc = 0; hc < CW / 8; ++hc) {
             __nv_bfloat16 ob[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) ob[j] = __float2bfloat16_rn(p.scale * x[8 * hc + j]);
+            for (int j = 0; j < 8; ++j) ob[j] = __float2bfloat16_rn(x[8 * hc + j]);
             dst[hc] = *reinterpret_cast<const uint4 *>(ob);
           }
         }
       }
-      umma::fence_proxy_async_smem();
-      umma::fence_before_sync();
-      umma::named_bar(kBarChain, kChainThreads);
+      if (tid < kChunk) {
+        umma::fence_proxy_async_smem();
+        umma::fence_before_sync();
+        umma::named_bar(kBarE, kChainThreads);
+      }
       if (tid == 0 && !bad) {   // D3 = k~^T U
         umma::fence_after_sync();
         const uint32_t id = umma::idesc_f16(128, BV, 1, 1);

@@ -253,6 +253,10 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool cond) {
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Arrival at a named barrier without waiting for it.
+__device__ __forceinline__ void named_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 }  // namespace umma
 }  // namespace kda
