@@ -28,6 +28,8 @@ SIGNATURES = {
     "kda_fwd": (I, [P, P, P, P, P, P, P, F, F, P, P, P, I, I, I, I, I, I, P, P, ctypes.c_size_t, P]),
     "kda_fwd_with_events": (I, [P, P, P, P, P, P, P, F, F, P, P, P, I, I, I, I, I, I, P, P, ctypes.c_size_t, P,
                                  P]),
+    "kda_fwd_ex": (I, [P, P, P, P, P, P, P, F, F, P, P, P, I, I, I, I, I, I, ctypes.c_uint32, P, P, ctypes.c_size_t,
+                        P, P]),
     "kda_fwd_noalloc": (I, [P, P, P, P, P, P, P, F, F, P, P, P, I, I, I, I, I, I, P, P]),
     "kda_debug_chunk_matrices": (I, [P, P, P, P, P, P, F, P, I, I, I, I, I, P, P, ctypes.c_size_t, P]),
     "kda_max_chunks": (ctypes.c_int64, [I, I, I]),

@@ -110,10 +110,17 @@ bool encode_token_map(CUtensorMap *m, const void *base, int D, int H, int T, int
 
 kda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
-// Shared argument checks of kda_fwd and kda_debug_chunk_matrices.
+static_assert(KDA_GATE_PER_HEAD == kda::kGatePerHead && KDA_BETA_F32 == kda::kBetaF32 &&
+                  KDA_STATE_BF16 == kda::kStateBf16 && KDA_STATE_KV == kda::kStateKV,
+              "variant flags of include/kda.h and the kernels");
+constexpr uint32_t kAllFlags = KDA_GATE_PER_HEAD | KDA_BETA_F32 | KDA_STATE_BF16 | KDA_STATE_KV;
+
+// Shared argument checks of kda_fwd_ex and kda_debug_chunk_matrices.
 kda_status_t check_common(const void *q, const void *k, const void *g, const void *beta,
                           const float *A_log, const float *dt_bias, float lower_bound,
-                          const int32_t *cu_seqlens, int B, int T, int H, int K, int num_seqs) {
+                          const int32_t *cu_seqlens, int B, int T, int H, int K, int num_seqs,
+                          uint32_t flags) {
+  if (flags & ~kAllFlags) return KDA_ERR_INVALID_ARG;
   if (!sizes_ok(B, T, H, K, K, num_seqs)) return KDA_ERR_INVALID_ARG;
   // token tensors may be null only when they hold no elements (T == 0)
   if (!A_log || (T > 0 && (!q || !k || !g || !beta))) return KDA_ERR_INVALID_ARG;
@@ -125,8 +132,10 @@ kda_status_t check_common(const void *q, const void *k, const void *g, const voi
   } else if (num_seqs != B) {
     return KDA_ERR_INVALID_ARG;
   }
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(g, 16) || !aligned(beta, 2) ||
-      !aligned(A_log, 4) || (dt_bias && !aligned(dt_bias, 16)))
+  const bool per_head = (flags & KDA_GATE_PER_HEAD) != 0;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(g, per_head ? 2 : 16) ||
+      !aligned(beta, (flags & KDA_BETA_F32) ? 4 : 2) || !aligned(A_log, 4) ||
+      (dt_bias && !aligned(dt_bias, per_head ? 4 : 16)))
     return KDA_ERR_INVALID_ARG;
   // element counts must fit the 64-bit index arithmetic of the kernels
   const double elems = (double)B * (double)T * (double)H * (double)K;
@@ -164,14 +173,15 @@ void release_scratch(Scratch &s, cudaStream_t stream) {
 kda_status_t fill_problem(kda::Problem &p, const Layout &L, void *ws, const void *q, const void *k,
                           const void *v, const void *g, const void *beta, const float *A_log,
                           const float *dt_bias, float lower_bound, float scale,
-                          const float *initial_state, float *final_state, const int32_t *cu,
-                          int B, int T, int H, int K, int V, int N, void *o) {
+                          const void *initial_state, void *final_state, const int32_t *cu,
+                          int B, int T, int H, int K, int V, int N, uint32_t flags, void *o) {
   std::memset(&p, 0, sizeof p);
   p.q = static_cast<const __nv_bfloat16 *>(q);
   p.k = static_cast<const __nv_bfloat16 *>(k);
   p.v = static_cast<const __nv_bfloat16 *>(v);
   p.g = static_cast<const __nv_bfloat16 *>(g);
-  p.beta = static_cast<const __nv_bfloat16 *>(beta);
+  p.beta = beta;
+  p.flags = flags;
   p.A_log = A_log;
   p.dt_bias = dt_bias;
   p.init = initial_state;
@@ -249,8 +259,18 @@ kda_status_t kda_fwd_with_events(const void *q, const void *k, const void *v, co
                                  int K, int V, int num_seqs, void *o, void *workspace,
                                  size_t workspace_bytes, kda_stream_t stream,
                                  const kda_stage_events_t *events) {
+  return kda_fwd_ex(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state, final_state,
+                    cu_seqlens, B, T, H, K, V, num_seqs, 0u, o, workspace, workspace_bytes, stream, events);
+}
+
+kda_status_t kda_fwd_ex(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                        const float *A_log, const float *dt_bias, float lower_bound, float scale,
+                        const void *initial_state, void *final_state, const int32_t *cu_seqlens, int B,
+                        int T, int H, int K, int V, int num_seqs, uint32_t flags, void *o,
+                        void *workspace, size_t workspace_bytes, kda_stream_t stream,
+                        const kda_stage_events_t *events) {
   kda_status_t st = check_common(q, k, g, beta, A_log, dt_bias, lower_bound, cu_seqlens, B, T, H, K,
-                                 num_seqs);
+                                 num_seqs, flags);
   if (st != KDA_OK) return st;
   if (V < 1) return KDA_ERR_INVALID_ARG;
   if (T > 0 && (!v || !o)) return KDA_ERR_INVALID_ARG;
@@ -267,7 +287,7 @@ kda_status_t kda_fwd_with_events(const void *q, const void *k, const void *v, co
   if (st != KDA_OK) return st;
   kda::Problem p;
   st = fill_problem(p, L, scr.ptr, q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
-                    final_state, cu_seqlens, B, T, H, K, V, num_seqs, o);
+                    final_state, cu_seqlens, B, T, H, K, V, num_seqs, flags, o);
   auto mark = [&](void *ev) {
     if (st == KDA_OK && ev) st = from_cuda(cudaEventRecord(static_cast<cudaEvent_t>(ev), s));
   };
@@ -316,7 +336,7 @@ kda_status_t kda_debug_chunk_matrices(const void *q, const void *k, const void *
                                       int num_seqs, void *chunk_mats, void *workspace,
                                       size_t workspace_bytes, kda_stream_t stream) {
   kda_status_t st = check_common(q, k, g, beta, A_log, dt_bias, lower_bound, cu_seqlens, B, T, H, K,
-                                 num_seqs);
+                                 num_seqs, 0u);
   if (st != KDA_OK) return st;
   if (!chunk_mats || !aligned(chunk_mats, 16)) return KDA_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -327,7 +347,7 @@ kda_status_t kda_debug_chunk_matrices(const void *q, const void *k, const void *
   if (st != KDA_OK) return st;
   kda::Problem p;
   st = fill_problem(p, L, scr.ptr, q, k, k, g, beta, A_log, dt_bias, lower_bound, 1.0f, nullptr, nullptr,
-                    cu_seqlens, B, T, H, K, K, num_seqs, nullptr);
+                    cu_seqlens, B, T, H, K, K, num_seqs, 0u, nullptr);
   p.mats = static_cast<__half *>(chunk_mats);
   p.mat_stride = 2 * kda::kChunk * kda::kChunk;
   if (st == KDA_OK && cu_seqlens) st = from_cuda(kda::launch_varlen_schedule(p, s));

@@ -24,11 +24,19 @@ constexpr int kDevOk = 0;
 constexpr int kDevBadCuSeqlens = 1;
 constexpr int kDevWaitTimeout = 2;
 
+// Variant flags (mirrors KDA_GATE_PER_HEAD, KDA_BETA_F32, KDA_STATE_BF16, KDA_STATE_KV in
+// include/kda.h).
+constexpr uint32_t kGatePerHead = 0x1u;   // g [B,T,H], dt_bias [H]: one decay per token and head
+constexpr uint32_t kBetaF32 = 0x2u;       // beta logits in fp32
+constexpr uint32_t kStateBf16 = 0x4u;     // initial / final state in bf16
+constexpr uint32_t kStateKV = 0x8u;       // state layout [N,H,K,V] instead of [N,H,V,K]
+
 struct Problem {
-  const __nv_bfloat16 *q, *k, *v, *g, *beta;
-  const float *A_log, *dt_bias;      // dt_bias may be null
-  const float *init;                 // [N,H,V,K] or null
-  float *final_state;                // [N,H,V,K] or null
+  const __nv_bfloat16 *q, *k, *v, *g;  // g [B,T,H,K], or [B,T,H] with kGatePerHead
+  const void *beta;                  // [B,T,H] logits, bf16 or fp32 (kBetaF32)
+  const float *A_log, *dt_bias;      // dt_bias [H,K] ([H] with kGatePerHead) or null
+  const void *init;                  // [N,H,V,K] or [N,H,K,V] (kStateKV), fp32 or bf16, or null
+  void *final_state;                 // same type and layout as init, or null
   const int32_t *cu;                 // [N+1] or null (fixed length)
   __nv_bfloat16 *o;                  // [B,T,H,V]
   // prep -> recurrence hand-off: one block per (chunk, head) slot s = chunk * H + head at
@@ -46,6 +54,7 @@ struct Problem {
   int B, T, H, K, V, N;
   int nc_fixed;                      // ceil(T / C) in fixed-length mode
   long long max_chunks;
+  uint32_t flags;                    // variant flags above
 };
 
 // TMA descriptor of v, viewed as 4D [B][T][H][V] (innermost V) with a box of
@@ -70,6 +79,21 @@ __host__ __device__ constexpr long long hand_off_qt(int K) { return kMatBytes + 
 __host__ __device__ constexpr long long hand_off_kt(int K) { return kMatBytes + 256ll * K; }
 __host__ __device__ constexpr long long hand_off_gam(int K) { return kMatBytes + 384ll * K; }
 __host__ __device__ constexpr long long hand_bytes(int K) { return (kMatBytes + 388ll * K + 255) / 256 * 256; }
+
+// Element index of S[k][v] of (sequence s, head h) in the state tensors, and the state's
+// load and store in its storage type (the state is fp32 inside the kernels).
+__device__ __forceinline__ long long state_index(const Problem &p, int s, int h, int k, int v) {
+  return (p.flags & kStateKV) ? (((long long)s * p.H + h) * p.K + k) * p.V + v
+                              : (((long long)s * p.H + h) * p.V + v) * p.K + k;
+}
+__device__ __forceinline__ float state_load(const Problem &p, long long i) {
+  return (p.flags & kStateBf16) ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.init)[i])
+                                : static_cast<const float *>(p.init)[i];
+}
+__device__ __forceinline__ void state_store(const Problem &p, long long i, float x) {
+  if (p.flags & kStateBf16) static_cast<__nv_bfloat16 *>(p.final_state)[i] = __float2bfloat16_rn(x);
+  else static_cast<float *>(p.final_state)[i] = x;
+}
 
 struct SeqInfo {
   int b;        // batch row

@@ -51,6 +51,8 @@
 // -T_[23] A_[23][01] T_[01] as 16 x 16 block products. Both write Tb = T diag(beta)
 // straight into the operand of M = [-I ; P] Tb, a second tensor-core product
 // (128 x 64 x 64).
+#include <type_traits>
+
 #include "kda_common.cuh"
 #include "umma.cuh"
 
@@ -127,7 +129,9 @@ __device__ __forceinline__ void st_half4(unsigned char *p, F4 v) {
   *reinterpret_cast<uint2 *>(p) = make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
 }
 
-template <int K>
+// PH: one gate per token and head (kGatePerHead); BF32: fp32 beta logits (kBetaF32). Separate
+// instantiations, so that the default kernel carries no code for them.
+template <int K, bool PH, bool BF32>
 __global__ void __launch_bounds__(kPrepThreads, 2)
 prep_kernel(const Problem p) {
   using Lay = PrepLayout;
@@ -200,13 +204,15 @@ prep_kernel(const Problem p) {
         rq[hf][r] = ldg_u64(p.q + off);
       }
     }
-    if (cq < 4 * (K / 64)) {   // g of the sub-block to L2: one prefetch per (row, 128-byte line)
+    if (!PH && cq < 4 * (K / 64)) {   // g of the sub-block to L2: one prefetch per (row, 128-byte line)
       const int r = cq / (K / 64), line = cq % (K / 64);
       asm volatile("prefetch.global.L2 [%0];" ::"l"(p.g + rbase + (long long)min(r, nrows - 1) * rstride + 64 * line));
     }
   }
-  __nv_bfloat16 beta_raw = __float2bfloat16(0.f);   // beta logit of token tid (tid < 64)
-  if (tid < len) beta_raw = p.beta[tok_row(p, si.b, t0 + tid, h)];
+  // beta logit of token tid (tid < 64), converted where it is used
+  using BetaT = typename std::conditional<BF32, float, __nv_bfloat16>::type;
+  BetaT beta_raw = BetaT(0.f);
+  if (tid < len) beta_raw = static_cast<const BetaT *>(p.beta)[tok_row(p, si.b, t0 + tid, h)];
   const float a_log = p.A_log[h];
 
   // ---- pass 0: TMEM, barrier
@@ -280,7 +286,10 @@ prep_kernel(const Problem p) {
 
 #pragma unroll 1
   for (int hf = 0; hf < K / 64; ++hf) {
-    // ---- pass 2a: gate and log decay of 4 rows x 4 channels (k and q as loaded by pass 1)
+    // ---- pass 2a: gate and log decay of 4 rows x 4 channels (k and q as loaded by pass 1). With
+    // one gate per token and head (kGatePerHead) g is [B,T,H]: its element index is the token
+    // row, and the row's pre-activation is shared by all channels.
+    constexpr bool per_head = PH;
     const int kk = 64 * hf + 4 * cq;
     uint2 rawk[4], rawq[4], rawg[4];
 #pragma unroll
@@ -288,7 +297,8 @@ prep_kernel(const Problem p) {
     if (nrows > 0) {   // no load at all when the whole sub-block is past the sequence end
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        rawg[r] = ldg_u64(p.g + row_off(r) + kk);
+        if (per_head) rawg[r].x = static_cast<uint32_t>(reinterpret_cast<const unsigned short &>(p.g[row_off(r) / K]));
+        else rawg[r] = ldg_u64(p.g + row_off(r) + kk);
         rawk[r] = (K == 128 && hf > 0) ? rk[K / 64 - 1][r] : rk[0][r];
         rawq[r] = (K == 128 && hf > 0) ? rq[K / 64 - 1][r] : rq[0][r];
       }
@@ -298,13 +308,14 @@ prep_kernel(const Problem p) {
       }
     }
     F4 dt = splat4(0.f);
-    if (p.dt_bias) dt = f4_of(*reinterpret_cast<const float4 *>(p.dt_bias + h * K + kk));
+    if (p.dt_bias) dt = per_head ? splat4(p.dt_bias[h]) : f4_of(*reinterpret_cast<const float4 *>(p.dt_bias + h * K + kk));
     const F4 cdt = mul4(splat4(cg), dt);
     F4 al[4], kv[4], qv[4];
     F4 ssum = splat4(0.f);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const F4 g4 = bf4_to_f4(rawg[r]);
+      // per head: the token's gate (low half of rawg[r].x) in every channel
+      const F4 g4 = per_head ? splat4(__uint_as_float(rawg[r].x << 16)) : bf4_to_f4(rawg[r]);
       const F4 e = {__ffma2_rn(make_float2(cg, cg), g4.lo, cdt.lo), __ffma2_rn(make_float2(cg, cg), g4.hi, cdt.hi)};
       F4 la = {make_float2(lbl2 * rcp_approx(1.f + ex2_approx(e.lo.x)), lbl2 * rcp_approx(1.f + ex2_approx(e.lo.y))),
                make_float2(lbl2 * rcp_approx(1.f + ex2_approx(e.hi.x)), lbl2 * rcp_approx(1.f + ex2_approx(e.hi.y)))};
@@ -315,7 +326,7 @@ prep_kernel(const Problem p) {
       qv[r] = bf4_to_f4(rawq[r]);
     }
     ms.ssub[J][sbi][cq] = float4_of(ssum);
-    if (hf == 0 && tid < kChunk) ms.beta[tid] = (tid < len) ? sigmoid_fast(__bfloat162float(beta_raw)) : 0.f;
+    if (hf == 0 && tid < kChunk) ms.beta[tid] = (tid < len) ? sigmoid_fast(static_cast<float>(beta_raw)) : 0.f;
     __syncthreads();
 
     // ---- pass 2b: operands of the A/P product for this half (tf32, rounded to nearest), and the
@@ -598,21 +609,28 @@ prep_kernel(const Problem p) {
   if (warp == 0) umma::tmem_dealloc(tmem, kPrepTmemCols);
 }
 
-template <int K>
+template <int K, bool PH, bool BF32>
 static cudaError_t launch_prep_t(const Problem &p, cudaStream_t stream) {
   using Lay = PrepLayout;
   const size_t smem = Lay::end + sizeof(PrepMisc) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(prep_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(prep_kernel<K, PH, BF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.max_chunks, (unsigned)p.H);
-  prep_kernel<K><<<grid, kPrepThreads, smem, stream>>>(p);
+  prep_kernel<K, PH, BF32><<<grid, kPrepThreads, smem, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int K>
+static cudaError_t launch_prep_k(const Problem &p, cudaStream_t stream) {
+  const bool ph = (p.flags & kGatePerHead) != 0, bf32 = (p.flags & kBetaF32) != 0;
+  if (ph) return bf32 ? launch_prep_t<K, true, true>(p, stream) : launch_prep_t<K, true, false>(p, stream);
+  return bf32 ? launch_prep_t<K, false, true>(p, stream) : launch_prep_t<K, false, false>(p, stream);
 }
 
 cudaError_t launch_prep(const Problem &p, cudaStream_t stream) {
   if (p.max_chunks == 0) return cudaSuccess;
-  return p.K == 64 ? launch_prep_t<64>(p, stream) : launch_prep_t<128>(p, stream);
+  return p.K == 64 ? launch_prep_k<64>(p, stream) : launch_prep_k<128>(p, stream);
 }
 
 }  // namespace kda

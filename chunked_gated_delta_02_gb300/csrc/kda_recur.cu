@@ -150,11 +150,13 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
     ms.err = 0;
   }
   // chain threads: state master S[k][0:BV] (fp32, thread k) and its fp16 operand copy
+  // (element index of S[tid][v0 + v] = st0 + v * stv in either state layout)
+  const int stv = (p.flags & kStateKV) ? 1 : K;
   float S[BV];
   if (is_chain && tid < K) {
+    const long long st0 = state_index(p, s, h, tid, v0);
 #pragma unroll
-    for (int v = 0; v < BV; ++v)
-      S[v] = p.init ? p.init[(((long long)s * p.H + h) * p.V + v0 + v) * K + tid] : 0.f;
+    for (int v = 0; v < BV; ++v) S[v] = p.init ? state_load(p, st0 + v * stv) : 0.f;
 #pragma unroll
     for (int c = 0; c < BV / 8; ++c) {
       uint4 w;
@@ -444,7 +446,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
     if (tid == 0) atomicExch(p.dev_status, kDevWaitTimeout);
   } else if (is_chain && p.final_state && tid < K) {
 #pragma unroll
-    for (int v = 0; v < BV; ++v) p.final_state[(((long long)s * p.H + h) * p.V + v0 + v) * K + tid] = S[v];
+    for (int v = 0; v < BV; ++v) state_store(p, state_index(p, s, h, tid, v0) + v * stv, S[v]);
   }
   if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
 }

@@ -2,9 +2,11 @@
 
 ``fwd`` mirrors the KDA forward call of the cuLA / FLA API (cuLA README mirror,
 "Quick Start"; FlashKDA page, "flash-linear-attention 백엔드로 사용"), with the
-in-kernel options fixed on: q/k L2 norm, gate activation with a lower bound,
-beta sigmoid, and the [N,H,V,K] state layout. All compute runs in libkda.so on
-the caller's current CUDA stream; torch only provides device memory.
+in-kernel options fixed on: q/k L2 norm, gate activation with a lower bound and
+beta sigmoid. The variants of kda_fwd_ex are chosen from the arguments: a
+[B,T,H] gate (one decay per token and head, the gated delta rule), fp32 beta
+logits, a bf16 state and the [N,H,K,V] state layout. All compute runs in
+libkda.so on the caller's current CUDA stream; torch only provides device memory.
 """
 from __future__ import annotations
 
@@ -16,10 +18,13 @@ import torch
 from ._lib import check, lib
 
 __all__ = ["fwd", "fwd_noalloc", "workspace_size", "debug_chunk_matrices", "device_status", "max_chunks",
-           "NOALLOC_MAX_SCRATCH"]
+           "NOALLOC_MAX_SCRATCH", "GATE_PER_HEAD", "BETA_F32", "STATE_BF16", "STATE_KV"]
 
 # Size of the library's fixed scratch array used by fwd_noalloc (KDA_NOALLOC_MAX_SCRATCH).
 NOALLOC_MAX_SCRATCH = 16 * 1024 * 1024
+
+# Variant flags of kda_fwd_ex (include/kda.h).
+GATE_PER_HEAD, BETA_F32, STATE_BF16, STATE_KV = 0x1, 0x2, 0x4, 0x8
 
 
 class _StageEvents(ctypes.Structure):
@@ -63,35 +68,58 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
         output_final_state: bool = False, cu_seqlens: Optional[torch.Tensor] = None,
         workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
         final_state: Optional[torch.Tensor] = None,
-        events=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+        events=None, state_layout: str = "vk",
+        state_dtype: Optional[torch.dtype] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """KDA chunked forward on the GPU.
 
-    q, k, g: bf16 [B,T,H,K]; v: bf16 [B,T,H,V]; beta: bf16 [B,T,H] logits;
-    A_log: fp32 [H]; dt_bias: fp32 [H,K] (or [H*K]) or None; initial_state:
-    fp32 [N,H,V,K] or None; cu_seqlens: int32 [N+1] or None (then B must be 1).
-    Returns (o bf16 [B,T,H,V], final_state fp32 [N,H,V,K] or None).
+    q, k: bf16 [B,T,H,K]; v: bf16 [B,T,H,V]; g: bf16 [B,T,H,K], or [B,T,H] for one
+    decay per token and head (then dt_bias is [H]); beta: bf16 or fp32 [B,T,H]
+    logits; A_log: fp32 [H]; dt_bias: fp32 [H,K] (or [H*K]) or None;
+    initial_state: [N,H,V,K] (state_layout "vk") or [N,H,K,V] ("kv"), fp32 or
+    bf16, or None; cu_seqlens: int32 [N+1] or None (then B must be 1).
+    state_dtype: dtype of the returned final state when there is no
+    initial_state (default fp32; with an initial_state, its dtype).
+    Returns (o bf16 [B,T,H,V], final_state in the state layout and dtype, or None).
     events: optional (prep_start, prep_done, recur_done) torch.cuda.Event triple
     recorded on the current stream at the kernel boundaries (profiling only).
     """
     B, T, H, K = q.shape
     V = v.shape[-1]
+    flags = 0
     _need(q, "q", torch.bfloat16)
     _need(k, "k", torch.bfloat16, (B, T, H, K))
-    _need(g, "g", torch.bfloat16, (B, T, H, K))
+    if g.dim() == 3:
+        flags |= GATE_PER_HEAD
+        _need(g, "g", torch.bfloat16, (B, T, H))
+    else:
+        _need(g, "g", torch.bfloat16, (B, T, H, K))
     _need(v, "v", torch.bfloat16, (B, T, H, V))
-    _need(beta, "beta", torch.bfloat16, (B, T, H))
+    if beta.dtype == torch.float32:
+        flags |= BETA_F32
+    _need(beta, "beta", beta.dtype if beta.dtype == torch.float32 else torch.bfloat16, (B, T, H))
     _need(A_log, "A_log", torch.float32, (H,))
     if dt_bias is not None:
         _need(dt_bias, "dt_bias", torch.float32)
-        if dt_bias.numel() != H * K:
-            raise ValueError("dt_bias must hold H*K values")
+        want = H if flags & GATE_PER_HEAD else H * K
+        if dt_bias.numel() != want:
+            raise ValueError(f"dt_bias must hold {want} values")
     if cu_seqlens is not None:
         _need(cu_seqlens, "cu_seqlens", torch.int32)
         N = cu_seqlens.numel() - 1
     else:
         N = B
+    if state_layout not in ("vk", "kv"):
+        raise ValueError("state_layout must be 'vk' ([N,H,V,K]) or 'kv' ([N,H,K,V])")
+    sshape = (N, H, V, K) if state_layout == "vk" else (N, H, K, V)
+    if state_layout == "kv":
+        flags |= STATE_KV
+    sdt = initial_state.dtype if initial_state is not None else (state_dtype or torch.float32)
+    if sdt not in (torch.float32, torch.bfloat16):
+        raise TypeError("the state must be float32 or bfloat16")
+    if sdt == torch.bfloat16:
+        flags |= STATE_BF16
     if initial_state is not None:
-        _need(initial_state, "initial_state", torch.float32, (N, H, V, K))
+        _need(initial_state, "initial_state", sdt, sshape)
     if scale is None:
         scale = K ** -0.5
     dev = q.device
@@ -99,9 +127,8 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
     _need(o, "out", torch.bfloat16, (B, T, H, V))
     fs = None
     if output_final_state:
-        fs = final_state if final_state is not None else torch.empty(N, H, V, K, dtype=torch.float32,
-                                                                     device=dev)
-        _need(fs, "final_state", torch.float32, (N, H, V, K))
+        fs = final_state if final_state is not None else torch.empty(*sshape, dtype=sdt, device=dev)
+        _need(fs, "final_state", sdt, sshape)
     need = workspace_size(B, T, H, K, V, N)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
@@ -112,11 +139,11 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
         ev = ctypes.byref(_StageEvents(*[ctypes.c_void_p(e.cuda_event if e is not None else 0)
                                          for e in events]))
     with torch.cuda.device(dev):
-        rc = lib().kda_fwd_with_events(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log),
-                                       _ptr(dt_bias), float(lower_bound), float(scale),
-                                       _ptr(initial_state), _ptr(fs), _ptr(cu_seqlens), B, T, H, K, V, N,
-                                       _ptr(o), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                       _stream_ptr(), ev)
+        rc = lib().kda_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log),
+                              _ptr(dt_bias), float(lower_bound), float(scale),
+                              _ptr(initial_state), _ptr(fs), _ptr(cu_seqlens), B, T, H, K, V, N, flags,
+                              _ptr(o), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _stream_ptr(), ev)
     check("kda_fwd", rc)
     return o, fs
 

@@ -125,6 +125,30 @@ KDA_API kda_status_t kda_fwd(const void *q, const void *k, const void *v, const 
                      size_t workspace_bytes, kda_stream_t stream);
 
 /*
+ * Variant flags of kda_fwd_ex() (bitwise OR; 0 is kda_fwd()):
+ *
+ *   KDA_GATE_PER_HEAD  one decay per token and head instead of per channel (the
+ *                      gated delta rule, GDN, of the cuLA overview and FlashQLA
+ *                      pages): g is bf16 [B,T,H] and dt_bias fp32 [H] (or NULL),
+ *                      and every channel k of head h takes
+ *                      log alpha_t = lower_bound * sigmoid(exp(A_log[h]) * (g[t,h] + dt_bias[h])).
+ *                      Alignment: g 2-byte, dt_bias 4-byte.
+ *   KDA_BETA_F32       beta holds fp32 logits [B,T,H] (the cuLA Quick Start
+ *                      notes: beta in float32 or bfloat16). Alignment 4-byte.
+ *   KDA_STATE_BF16     initial_state and final_state are bf16 instead of fp32
+ *                      (the FlashKDA parameter table: bf16/fp32 state). The
+ *                      state is carried in fp32 inside; only its load and store
+ *                      change, the store rounding to nearest-even.
+ *   KDA_STATE_KV       initial_state and final_state are laid out [N,H,K,V]
+ *                      (state[s,h,k,v] = S[k,v], the layout of the cuLA usage
+ *                      example) instead of [N,H,V,K].
+ */
+#define KDA_GATE_PER_HEAD 0x1u
+#define KDA_BETA_F32 0x2u
+#define KDA_STATE_BF16 0x4u
+#define KDA_STATE_KV 0x8u
+
+/*
  * Stage timing hooks for kda_fwd_with_events(): CUDA events (cudaEvent_t,
  * created by the caller) recorded on `stream` at the stage boundaries. Any
  * member may be NULL. prep_start precedes the varlen schedule (if any) and
@@ -151,6 +175,22 @@ KDA_API kda_status_t kda_fwd_with_events(const void *q, const void *k, const voi
                                          int H, int K, int V, int num_seqs, void *o, void *workspace,
                                          size_t workspace_bytes, kda_stream_t stream,
                                          const kda_stage_events_t *events);
+
+/*
+ * kda_fwd_with_events() with variant flags (KDA_GATE_PER_HEAD, KDA_BETA_F32,
+ * KDA_STATE_BF16, KDA_STATE_KV, above). The state pointers are untyped: fp32
+ * or bf16 by KDA_STATE_BF16, [N,H,V,K] or [N,H,K,V] by KDA_STATE_KV; every
+ * other argument, layout, alignment rule and error is that of kda_fwd(), except
+ * where a flag states otherwise. Unknown flag bits give KDA_ERR_INVALID_ARG.
+ * kda_fwd(...) is kda_fwd_ex(..., 0, ...) with events NULL.
+ */
+KDA_API kda_status_t kda_fwd_ex(const void *q, const void *k, const void *v, const void *g,
+                                const void *beta, const float *A_log, const float *dt_bias,
+                                float lower_bound, float scale, const void *initial_state,
+                                void *final_state, const int32_t *cu_seqlens, int B, int T, int H,
+                                int K, int V, int num_seqs, uint32_t flags, void *o, void *workspace,
+                                size_t workspace_bytes, kda_stream_t stream,
+                                const kda_stage_events_t *events);
 
 /*
  * Diagnostic entry point: runs only the varlen schedule and the token-parallel

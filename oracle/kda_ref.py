@@ -31,6 +31,11 @@ Readings where the pages are silent (each is also listed in the design notes):
   * with cu_seqlens, B must be 1 and each sequence starts from its own
     initial_state row; a zero-length sequence leaves its state unchanged.
   * sigmoid(+inf) = 1 and sigmoid(-inf) = 0 exactly.
+  * the gated delta rule (GDN, named on the cuLA overview and FlashQLA pages
+    without its formulas) is read as KDA with one decay per token and head: g
+    is [B,T,H] and dt_bias [H], and every channel of the head takes the same
+    log alpha = lower_bound * sigmoid(exp(A_log[h]) * (g[t,h] + dt_bias[h])).
+    Diag(alpha) is then alpha I.
 """
 from __future__ import annotations
 
@@ -105,7 +110,9 @@ def kda_fwd_ref(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
 
     Arguments are arrays (torch or numpy) with the layouts of the module doc:
     q, k, g [B,T,H,K]; v [B,T,H,V]; beta [B,T,H]; A_log [H]; dt_bias [H,K] or
-    None; initial_state [N,H,V,K] or None; cu_seqlens [N+1] or None.
+    None; initial_state [N,H,V,K] or None; cu_seqlens [N+1] or None. A gate g
+    of shape [B,T,H] (with dt_bias [H] or None) is one decay per token and
+    head, the same in every channel.
 
     Returns (o, final_state): o float64 [B,T,H,V] (rows of heads not in
     ``heads`` are left at zero), final_state float64 [N,H,V,K].
@@ -114,6 +121,9 @@ def kda_fwd_ref(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
     A_log = to_f64(A_log)
     B, T, H, K = q.shape
     V = v.shape[-1]
+    if g.ndim == 3:   # one gate per token and head: the same value in every channel
+        g = np.repeat(g[..., None], K, axis=-1)
+        dt_bias = None if dt_bias is None else np.repeat(to_f64(dt_bias).reshape(H, 1), K, axis=1)
     dt_bias = np.zeros((H, K)) if dt_bias is None else to_f64(dt_bias).reshape(H, K)
     seqs = _sequences(B, T, cu_seqlens)
     if cu_seqlens is not None and B != 1:

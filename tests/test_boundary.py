@@ -107,3 +107,35 @@ def test_debug_wait_timeout_rejects_bad_limits_without_launch(lib):
     assert lib.kda_debug_wait_timeout(0, None) == 1
     assert lib.kda_debug_wait_timeout(-5, None) == 1
     assert lib.kda_debug_wait_timeout(1 << 32, None) == 1
+
+
+def _call_ex(lib, flags, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, A_log=FAKE, dt_bias=None, lb=-5.0, scale=0.125,
+             init=None, final=None, cu=None, B=1, T=64, H=1, K=64, V=64, N=1, o=FAKE, ws=FAKE,
+             ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.kda_fwd_ex(a["q"], a["k"], a["v"], a["g"], a["beta"], a["A_log"], a["dt_bias"], a["lb"],
+                          a["scale"], a["init"], a["final"], a["cu"], a["B"], a["T"], a["H"], a["K"],
+                          a["V"], a["N"], flags, a["o"], a["ws"], a["ws_bytes"], a["stream"], None)
+
+
+def test_fwd_ex_rejects_unknown_flags_without_launch(lib):
+    for flags in (0x10, 0x80000000, 0x1F):
+        assert _call_ex(lib, flags) == 1
+
+
+def test_fwd_ex_variant_alignment_rules(lib):
+    GATE_PER_HEAD, BETA_F32 = 0x1, 0x2
+    # per-channel gate and dt_bias need 16-byte alignment; per head only their element size
+    assert _call_ex(lib, 0, g=FAKE + 2) == 1
+    assert _call_ex(lib, GATE_PER_HEAD, g=FAKE + 1) == 1
+    assert _call_ex(lib, 0, dt_bias=FAKE + 4) == 1
+    assert _call_ex(lib, GATE_PER_HEAD, dt_bias=FAKE + 2) == 1
+    # fp32 beta needs 4-byte alignment, bf16 beta 2-byte
+    assert _call_ex(lib, BETA_F32, beta=FAKE + 2) == 1
+    assert _call_ex(lib, 0, beta=FAKE + 1) == 1
+    # the other checks still apply under every flag
+    for flags in (0x1, 0x2, 0x4, 0x8, 0xF):
+        assert _call_ex(lib, flags, K=96) == 2          # unsupported head dim
+        assert _call_ex(lib, flags, lb=-6.0) == 1       # lower bound out of range
+        assert _call_ex(lib, flags, init=FAKE + 8) == 1  # state alignment

@@ -419,3 +419,76 @@ def test_pins_catch_planted_mistake(mutation):
         except (AssertionError, ValueError, IndexError):
             caught.append(pin.__name__)
     assert caught, f"no pin catches mutation {mutation}"
+
+
+# --------------------------------------------------------------------------- per-head gate
+# The gated delta rule variant: g [B,T,H] and dt_bias [H], one decay per token and head
+# (the oracle's reading of the GDN pages). The numpy oracle takes it directly; these pins tie
+# it to closed forms and to a differently ordered scalar-decay recurrence written here.
+def _per_head_inputs(rng, B=2, T=23, H=2, K=6, V=5, lb=-2.0, init=True):
+    inp = rand_inputs(rng, B=B, T=T, H=H, K=K, V=V, lb=lb, init=init)
+    inp["g"] = _bf(0.7 * rng.standard_normal((B, T, H)))
+    inp["dt_bias"] = _f32(0.2 * rng.standard_normal(H))
+    return inp
+
+
+def test_per_head_gate_decay_only_closed_form():
+    # beta = 0 leaves only the decay. With A_log = 0 and dt_bias = 0 the special gate values
+    # g = 0, +huge, -huge give sigmoid = 1/2, 1, 0, i.e. alpha = e^{lb/2}, e^{lb}, 1 exactly, so
+    # S_t = (prod alpha) S0 and o_t = scale (prod alpha) S0^T q_hat.
+    rng = np.random.default_rng(RNG_SEED + 40)
+    B, T, H, K, V, lb = 1, 12, 2, 5, 4, -3.0
+    inp = _per_head_inputs(rng, B, T, H, K, V, lb)
+    codes = rng.integers(0, 3, size=(B, T, H))
+    inp["g"] = np.choose(codes, [0.0, 1e30, -1e30]).astype(np.float64)
+    inp["A_log"] = np.zeros(H)
+    inp["dt_bias"] = np.zeros(H)
+    inp["beta"] = np.full_like(inp["beta"], -np.inf)
+    o, f = impl_numpy(inp, 1e-6)
+    log_alpha = np.choose(codes, [lb / 2, lb, 0.0])
+    cum = np.cumsum(log_alpha, axis=1)                          # [B,T,H]
+    q = inp["q"]
+    qh = q / np.sqrt(np.linalg.norm(q, axis=-1, keepdims=True) ** 2 + 1e-6)
+    for h in range(H):
+        S0 = inp["initial_state"][0, h].T                       # K x V
+        exp_o = inp["scale"] * np.exp(cum[0, :, h])[:, None] * (qh[0, :, h] @ S0)
+        _close(o[0, :, h], exp_o, 1e-12, 1e-14, f"per-head decay-only o, head {h}")
+        _close(f[0, h], np.exp(cum[0, -1, h]) * inp["initial_state"][0, h], 1e-12, 1e-14,
+               f"per-head decay-only final, head {h}")
+
+
+def test_per_head_gate_matches_scalar_decay_recurrence():
+    # With a scalar decay alpha, Diag(alpha) = alpha I commutes with the projection, so the update
+    # may apply it after the delta-rule correction: S_t = alpha_t (S - beta_t k (k^T S)) + beta_t k v^T.
+    rng = np.random.default_rng(RNG_SEED + 41)
+    B, T, H, K, V, lb = 2, 19, 2, 6, 5, -1.5
+    inp = _per_head_inputs(rng, B, T, H, K, V, lb)
+    o, f = impl_numpy(inp, 1e-6)
+    for b in range(B):
+        for h in range(H):
+            S = inp["initial_state"][b, h].T.copy()
+            for t in range(T):
+                a = math.exp(inp["A_log"][h]) * (inp["g"][b, t, h] + inp["dt_bias"][h])
+                alpha = math.exp(lb / (1.0 + math.exp(-a)))
+                kv = inp["k"][b, t, h]
+                kh = kv / math.sqrt(float(kv @ kv) + 1e-6)
+                qv = inp["q"][b, t, h]
+                qh = qv / math.sqrt(float(qv @ qv) + 1e-6)
+                bt = 1.0 / (1.0 + math.exp(-inp["beta"][b, t, h]))
+                S = alpha * (S - bt * np.outer(kh, kh @ S)) + bt * np.outer(kh, inp["v"][b, t, h])
+                _close(o[b, t, h], inp["scale"] * (qh @ S), 1e-11, 1e-13, f"o b={b} t={t} h={h}")
+            _close(f[b, h], S.T, 1e-11, 1e-13, f"final b={b} h={h}")
+
+
+def test_per_head_gate_equals_channel_broadcast():
+    # The per-head gate is the per-channel oracle with g and dt_bias repeated over the channels,
+    # cross-checked on the plain-C oracle (exact bf16 / fp32 inputs).
+    rng = np.random.default_rng(RNG_SEED + 42)
+    inp = _per_head_inputs(rng, B=1, T=17, H=3, K=4, V=3, lb=-4.0)
+    o, f = impl_numpy(inp, 1e-6)
+    full = dict(inp)
+    full["g"] = np.repeat(inp["g"][..., None], 4, axis=-1)
+    full["dt_bias"] = np.repeat(inp["dt_bias"][:, None], 4, axis=1)
+    oc, fc = impl_c(full, 1e-6)
+    _close(o, oc, 1e-12, 1e-14, "per-head o vs broadcast C oracle")
+    _close(f, fc, 1e-12, 1e-14, "per-head final vs broadcast C oracle")
