@@ -111,9 +111,10 @@ bool encode_token_map(CUtensorMap *m, const void *base, int D, int H, int T, int
 kda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
 static_assert(KDA_GATE_PER_HEAD == kda::kGatePerHead && KDA_BETA_F32 == kda::kBetaF32 &&
-                  KDA_STATE_BF16 == kda::kStateBf16 && KDA_STATE_KV == kda::kStateKV,
+                  KDA_STATE_BF16 == kda::kStateBf16 && KDA_STATE_KV == kda::kStateKV &&
+                  KDA_EXP2_POLY == kda::kExp2Poly,
               "variant flags of include/kda.h and the kernels");
-constexpr uint32_t kAllFlags = KDA_GATE_PER_HEAD | KDA_BETA_F32 | KDA_STATE_BF16 | KDA_STATE_KV;
+constexpr uint32_t kAllFlags = KDA_GATE_PER_HEAD | KDA_BETA_F32 | KDA_STATE_BF16 | KDA_STATE_KV | KDA_EXP2_POLY;
 
 // Shared argument checks of kda_fwd_ex and kda_debug_chunk_matrices.
 kda_status_t check_common(const void *q, const void *k, const void *g, const void *beta,

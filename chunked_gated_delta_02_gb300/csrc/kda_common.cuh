@@ -13,6 +13,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "exp2_poly.cuh"
+
 namespace kda {
 
 constexpr int kChunk = 64;          // tokens per chunk
@@ -30,6 +32,7 @@ constexpr uint32_t kGatePerHead = 0x1u;   // g [B,T,H], dt_bias [H]: one decay p
 constexpr uint32_t kBetaF32 = 0x2u;       // beta logits in fp32
 constexpr uint32_t kStateBf16 = 0x4u;     // initial / final state in bf16
 constexpr uint32_t kStateKV = 0x8u;       // state layout [N,H,K,V] instead of [N,H,V,K]
+constexpr uint32_t kExp2Poly = 0x10u;     // per-token decays 2^la by a polynomial on the FMA pipe
 
 struct Problem {
   const __nv_bfloat16 *q, *k, *v, *g;  // g [B,T,H,K], or [B,T,H] with kGatePerHead
@@ -127,6 +130,26 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^x on the FMA pipe instead of the SFU, for x >= -126 (smaller x give 0, as the flush-to-zero
+// ex2.approx does): n = round(x) by adding and subtracting 1.5 * 2^23 (the sum's low mantissa bits
+// hold round(x)), f = x - n in [-1/2, 1/2], 2^f by the fitted polynomial of exp2_poly.cuh in
+// Horner form, and 2^n added to the exponent field. Relative error about 1.1e-7 plus the
+// rounding of five fused multiply-adds.
+__device__ __forceinline__ float ex2_poly(float x) {
+  const float xc = fmaxf(x, -126.f);
+  const float t = xc + 12582912.f;
+  const float f = xc - (t - 12582912.f);
+  float p = kExp2PolyC5;
+  p = fmaf(p, f, kExp2PolyC4);
+  p = fmaf(p, f, kExp2PolyC3);
+  p = fmaf(p, f, kExp2PolyC2);
+  p = fmaf(p, f, kExp2PolyC1);
+  p = fmaf(p, f, kExp2PolyC0);
+  const uint32_t n = (uint32_t)(__float_as_int(t) - 0x4B400000);   // round(x) (two's complement)
+  const float r = __int_as_float((int)((uint32_t)__float_as_int(p) + (n << 23)));
+  return x < -126.f ? 0.f : r;
 }
 
 __device__ __forceinline__ float rcp_approx(float x) {

@@ -129,11 +129,13 @@ __device__ __forceinline__ void st_half4(unsigned char *p, F4 v) {
   *reinterpret_cast<uint2 *>(p) = make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
 }
 
-// PH: one gate per token and head (kGatePerHead); BF32: fp32 beta logits (kBetaF32). Separate
-// instantiations, so that the default kernel carries no code for them.
-template <int K, bool PH, bool BF32>
+// VF: the variant flags that change this kernel's code: kGatePerHead (one gate per token and
+// head), kBetaF32 (fp32 beta logits), kExp2Poly (the per-token decays 2^la on the FMA pipe).
+// Separate instantiations, so that the default kernel carries no code for them.
+template <int K, uint32_t VF>
 __global__ void __launch_bounds__(kPrepThreads, 2)
 prep_kernel(const Problem p) {
+  constexpr bool PH = (VF & kGatePerHead) != 0, BF32 = (VF & kBetaF32) != 0, POLY = (VF & kExp2Poly) != 0;
   using Lay = PrepLayout;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // 1024-byte aligned base, derived from the __shared__ array by pointer arithmetic so that the
@@ -321,7 +323,9 @@ prep_kernel(const Problem p) {
                make_float2(lbl2 * rcp_approx(1.f + ex2_approx(e.hi.x)), lbl2 * rcp_approx(1.f + ex2_approx(e.hi.y)))};
       if (r >= nrows) la = splat4(0.f);
       ssum = add4(ssum, la);
-      al[r] = ex2_4(la);
+      if constexpr (POLY) al[r] = {make_float2(ex2_poly(la.lo.x), ex2_poly(la.lo.y)),
+                                   make_float2(ex2_poly(la.hi.x), ex2_poly(la.hi.y))};
+      else al[r] = ex2_4(la);
       kv[r] = bf4_to_f4(rawk[r]);
       qv[r] = bf4_to_f4(rawq[r]);
     }
@@ -609,23 +613,31 @@ prep_kernel(const Problem p) {
   if (warp == 0) umma::tmem_dealloc(tmem, kPrepTmemCols);
 }
 
-template <int K, bool PH, bool BF32>
+template <int K, uint32_t VF>
 static cudaError_t launch_prep_t(const Problem &p, cudaStream_t stream) {
   using Lay = PrepLayout;
   const size_t smem = Lay::end + sizeof(PrepMisc) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(prep_kernel<K, PH, BF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(prep_kernel<K, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.max_chunks, (unsigned)p.H);
-  prep_kernel<K, PH, BF32><<<grid, kPrepThreads, smem, stream>>>(p);
+  prep_kernel<K, VF><<<grid, kPrepThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 template <int K>
 static cudaError_t launch_prep_k(const Problem &p, cudaStream_t stream) {
-  const bool ph = (p.flags & kGatePerHead) != 0, bf32 = (p.flags & kBetaF32) != 0;
-  if (ph) return bf32 ? launch_prep_t<K, true, true>(p, stream) : launch_prep_t<K, true, false>(p, stream);
-  return bf32 ? launch_prep_t<K, false, true>(p, stream) : launch_prep_t<K, false, false>(p, stream);
+  constexpr uint32_t G = kGatePerHead, B = kBetaF32, X = kExp2Poly;
+  switch (p.flags & (G | B | X)) {
+    case 0: return launch_prep_t<K, 0>(p, stream);
+    case G: return launch_prep_t<K, G>(p, stream);
+    case B: return launch_prep_t<K, B>(p, stream);
+    case G | B: return launch_prep_t<K, G | B>(p, stream);
+    case X: return launch_prep_t<K, X>(p, stream);
+    case G | X: return launch_prep_t<K, G | X>(p, stream);
+    case B | X: return launch_prep_t<K, B | X>(p, stream);
+    default: return launch_prep_t<K, G | B | X>(p, stream);
+  }
 }
 
 cudaError_t launch_prep(const Problem &p, cudaStream_t stream) {

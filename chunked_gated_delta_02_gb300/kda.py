@@ -18,13 +18,13 @@ import torch
 from ._lib import check, lib
 
 __all__ = ["fwd", "fwd_noalloc", "workspace_size", "debug_chunk_matrices", "device_status", "max_chunks",
-           "NOALLOC_MAX_SCRATCH", "GATE_PER_HEAD", "BETA_F32", "STATE_BF16", "STATE_KV"]
+           "NOALLOC_MAX_SCRATCH", "GATE_PER_HEAD", "BETA_F32", "STATE_BF16", "STATE_KV", "EXP2_POLY"]
 
 # Size of the library's fixed scratch array used by fwd_noalloc (KDA_NOALLOC_MAX_SCRATCH).
 NOALLOC_MAX_SCRATCH = 16 * 1024 * 1024
 
 # Variant flags of kda_fwd_ex (include/kda.h).
-GATE_PER_HEAD, BETA_F32, STATE_BF16, STATE_KV = 0x1, 0x2, 0x4, 0x8
+GATE_PER_HEAD, BETA_F32, STATE_BF16, STATE_KV, EXP2_POLY = 0x1, 0x2, 0x4, 0x8, 0x10
 
 
 class _StageEvents(ctypes.Structure):
@@ -69,7 +69,8 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
         workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
         final_state: Optional[torch.Tensor] = None,
         events=None, state_layout: str = "vk",
-        state_dtype: Optional[torch.dtype] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+        state_dtype: Optional[torch.dtype] = None,
+        exp2_poly: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """KDA chunked forward on the GPU.
 
     q, k: bf16 [B,T,H,K]; v: bf16 [B,T,H,V]; g: bf16 [B,T,H,K], or [B,T,H] for one
@@ -79,13 +80,15 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
     bf16, or None; cu_seqlens: int32 [N+1] or None (then B must be 1).
     state_dtype: dtype of the returned final state when there is no
     initial_state (default fp32; with an initial_state, its dtype).
+    exp2_poly: evaluate the per-token decays with the FMA-pipe polynomial
+    instead of the SFU exponential (an implementation option, KDA_EXP2_POLY).
     Returns (o bf16 [B,T,H,V], final_state in the state layout and dtype, or None).
     events: optional (prep_start, prep_done, recur_done) torch.cuda.Event triple
     recorded on the current stream at the kernel boundaries (profiling only).
     """
     B, T, H, K = q.shape
     V = v.shape[-1]
-    flags = 0
+    flags = EXP2_POLY if exp2_poly else 0
     _need(q, "q", torch.bfloat16)
     _need(k, "k", torch.bfloat16, (B, T, H, K))
     if g.dim() == 3:

@@ -142,11 +142,19 @@ KDA_API kda_status_t kda_fwd(const void *q, const void *k, const void *v, const 
  *   KDA_STATE_KV       initial_state and final_state are laid out [N,H,K,V]
  *                      (state[s,h,k,v] = S[k,v], the layout of the cuLA usage
  *                      example) instead of [N,H,V,K].
+ *   KDA_EXP2_POLY      an implementation option, not a variant of the operation:
+ *                      the per-token, per-channel decays alpha = 2^(log2 alpha)
+ *                      are evaluated by a polynomial on the FMA pipe instead of
+ *                      the SFU exponential (the polynomial exponential of the
+ *                      cuLA launch blog, section "Status & Roadmap"). Results agree within
+ *                      the same tolerances; it is off by default because the
+ *                      prep kernel measured slower with it on GB300.
  */
 #define KDA_GATE_PER_HEAD 0x1u
 #define KDA_BETA_F32 0x2u
 #define KDA_STATE_BF16 0x4u
 #define KDA_STATE_KV 0x8u
+#define KDA_EXP2_POLY 0x10u
 
 /*
  * Stage timing hooks for kda_fwd_with_events(): CUDA events (cudaEvent_t,

@@ -120,7 +120,7 @@ def _call_ex(lib, flags, **kw):
 
 
 def test_fwd_ex_rejects_unknown_flags_without_launch(lib):
-    for flags in (0x10, 0x80000000, 0x1F):
+    for flags in (0x20, 0x80000000, 0x3F):
         assert _call_ex(lib, flags) == 1
 
 
@@ -135,7 +135,7 @@ def test_fwd_ex_variant_alignment_rules(lib):
     assert _call_ex(lib, BETA_F32, beta=FAKE + 2) == 1
     assert _call_ex(lib, 0, beta=FAKE + 1) == 1
     # the other checks still apply under every flag
-    for flags in (0x1, 0x2, 0x4, 0x8, 0xF):
+    for flags in (0x1, 0x2, 0x4, 0x8, 0x10, 0x1F):
         assert _call_ex(lib, flags, K=96) == 2          # unsupported head dim
         assert _call_ex(lib, flags, lb=-6.0) == 1       # lower bound out of range
         assert _call_ex(lib, flags, init=FAKE + 8) == 1  # state alignment

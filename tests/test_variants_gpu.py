@@ -117,3 +117,30 @@ def test_all_variants_wide_slices():
     w = custom(B=4, T=100, H=32, K=64, V=64, lower_bound=-5.0)
     inp = _variant_inputs(w, seed=33, per_head=True, beta_f32=True, state_bf16=True)
     _check(inp, "all variants, wide slices", layout="kv", bf16_state=True)
+
+
+@pytest.mark.parametrize("w", [custom(B=2, T=130, H=3, K=128, V=128, lower_bound=-5.0),
+                               custom(H=2, K=64, V=64, seqlens=[0, 1, 63, 64, 65, 150, 7], lower_bound=-1.0)],
+                         ids=["fixed-K128", "varlen-K64"])
+def test_exp2_poly_option(w):
+    import chunked_gated_delta_02_gb300 as kda
+    inp = _variant_inputs(w, seed=17)
+    d = to_dev(inp)
+    o, fs = kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"], d["lower_bound"],
+                    d["scale"], d["initial_state"], True, d["cu_seqlens"], exp2_poly=True)
+    torch.cuda.synchronize()
+    ref_o, ref_f = _oracle(inp)
+    eo, mo, es = assert_parity(o, fs, ref_o, ref_f, "exp2 polynomial")
+    print(f"exp2 polynomial: o rel {eo:.2e} maxabs {mo:.2e} state rel {es:.2e}")
+
+
+def test_exp2_poly_with_per_head_gate():
+    w = custom(B=1, T=200, H=2, K=128, V=64, lower_bound=-3.0)
+    inp = _variant_inputs(w, seed=19, per_head=True, beta_f32=True)
+    import chunked_gated_delta_02_gb300 as kda
+    d = to_dev(inp)
+    o, fs = kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"], d["lower_bound"],
+                    d["scale"], d["initial_state"], True, d["cu_seqlens"], exp2_poly=True)
+    torch.cuda.synchronize()
+    ref_o, ref_f = _oracle(inp)
+    assert_parity(o, fs, ref_o, ref_f, "exp2 polynomial, per-head gate, fp32 beta")
