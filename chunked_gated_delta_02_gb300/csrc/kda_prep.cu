@@ -301,33 +301,44 @@ prep_kernel(const Problem p) {
       for (int r = 0; r < 4; ++r) {
         if (per_head) rawg[r].x = static_cast<uint32_t>(reinterpret_cast<const unsigned short &>(p.g[row_off(r) / K]));
         else rawg[r] = ldg_u64(p.g + row_off(r) + kk);
-        rawk[r] = (K == 128 && hf > 0) ? rk[K / 64 - 1][r] : rk[0][r];
-        rawq[r] = (K == 128 && hf > 0) ? rq[K / 64 - 1][r] : rq[0][r];
-      }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        if (r >= nrows) rawk[r] = rawq[r] = rawg[r] = make_uint2(0u, 0u);
+        rawk[r] = rk[0][r];   // this half's k and q (the second half is moved down after the first)
+        rawq[r] = rq[0][r];
       }
     }
     F4 dt = splat4(0.f);
     if (p.dt_bias) dt = per_head ? splat4(p.dt_bias[h]) : f4_of(*reinterpret_cast<const float4 *>(p.dt_bias + h * K + kk));
     const F4 cdt = mul4(splat4(cg), dt);
-    F4 al[4], kv[4], qv[4];
+    F4 al[4], kv[4], qv[4], la[4];
     F4 ssum = splat4(0.f);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       // per head: the token's gate (low half of rawg[r].x) in every channel
       const F4 g4 = per_head ? splat4(__uint_as_float(rawg[r].x << 16)) : bf4_to_f4(rawg[r]);
       const F4 e = {__ffma2_rn(make_float2(cg, cg), g4.lo, cdt.lo), __ffma2_rn(make_float2(cg, cg), g4.hi, cdt.hi)};
-      F4 la = {make_float2(lbl2 * rcp_approx(1.f + ex2_approx(e.lo.x)), lbl2 * rcp_approx(1.f + ex2_approx(e.lo.y))),
+      la[r] = {make_float2(lbl2 * rcp_approx(1.f + ex2_approx(e.lo.x)), lbl2 * rcp_approx(1.f + ex2_approx(e.lo.y))),
                make_float2(lbl2 * rcp_approx(1.f + ex2_approx(e.hi.x)), lbl2 * rcp_approx(1.f + ex2_approx(e.hi.y)))};
-      if (r >= nrows) la = splat4(0.f);
-      ssum = add4(ssum, la);
-      if constexpr (POLY) al[r] = {make_float2(ex2_poly(la.lo.x), ex2_poly(la.lo.y)),
-                                   make_float2(ex2_poly(la.hi.x), ex2_poly(la.hi.y))};
-      else al[r] = ex2_4(la);
       kv[r] = bf4_to_f4(rawk[r]);
       qv[r] = bf4_to_f4(rawq[r]);
+    }
+    // rows past the sequence end (their k and q repeat the last row's, or are zero) decay nothing
+    if (nrows < 4) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        if (r >= nrows) la[r] = splat4(0.f);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      ssum = add4(ssum, la[r]);
+      if constexpr (POLY) al[r] = {make_float2(ex2_poly(la[r].lo.x), ex2_poly(la[r].lo.y)),
+                                   make_float2(ex2_poly(la[r].hi.x), ex2_poly(la[r].hi.y))};
+      else al[r] = ex2_4(la[r]);
+    }
+    if constexpr (K == 128) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        rk[0][r] = rk[K / 64 - 1][r];
+        rq[0][r] = rq[K / 64 - 1][r];
+      }
     }
     ms.ssub[J][sbi][cq] = float4_of(ssum);
     if (hf == 0 && tid < kChunk) ms.beta[tid] = (tid < len) ? sigmoid_fast(static_cast<float>(beta_raw)) : 0.f;
@@ -367,28 +378,30 @@ prep_kernel(const Problem p) {
       x1 = ex2_4(Bm[2]);
     }
     const int xrow = ((J == 0) ? 128 : 144) + 4 * sbi, yrow = 160 + 4 * sbi;
+    const float4 kn4 = *reinterpret_cast<const float4 *>(&ms.kn[row0]);   // this thread's four rows
+    const float4 qn4 = *reinterpret_cast<const float4 *>(&ms.qn[row0]);
+    const float knr[4] = {kn4.x, kn4.y, kn4.z, kn4.w};
+    const float qnr[4] = {qn4.x * p.scale, qn4.y * p.scale, qn4.z * p.scale, qn4.w * p.scale};
     if (hf > 0) wait_mma();   // the previous half's product has read the operands
 #pragma unroll
     for (int r = 0; r < 4; ++r) {   // I side; Gamma = X 2^{blocks before J}
-      const int i = row0 + r;
       X = mul4(X, al[r]);
-      st_tf32x4(opA_at(0, r), mul4(kv[r], X));
-      st_tf32x4(opA_at(64, r), mul4(qv[r], X));
-      const F4 G = mul4(X, PJ);
+      const F4 kx = mul4(kv[r], X), qx = mul4(qv[r], X);
+      st_tf32x4(opA_at(0, r), kx);
+      st_tf32x4(opA_at(64, r), qx);
       const uint32_t io = img_off(r);
-      st_half4(kg_img + io, mul4(kv[r], mul4(G, splat4(ms.kn[i]))));
-      st_half4(qt_img + io, mul4(qv[r], mul4(G, splat4(ms.qn[i] * p.scale))));
+      st_half4(kg_img + io, mul4(kx, mul4(PJ, splat4(knr[r]))));
+      st_half4(qt_img + io, mul4(qx, mul4(PJ, splat4(qnr[r]))));
     }
 #pragma unroll
     for (int r = 3; r >= 0; --r) {  // J side; Gamma_last / Gamma = Ys 2^{blocks after J}
-      const int i = row0 + r;
       const F4 ys = mul4(kv[r], suf);
       suf = mul4(suf, al[r]);
       st_tf32x4(opB_at(0, r), mul4(ys, eBinv));
       st_tf32x4(opB_at(64, r), ys);
       if (J < 2) st_tf32x4(opB_at(xrow - row0, r), mul4(ys, x1));
       if (J == 0) st_tf32x4(opB_at(yrow - row0, r), mul4(ys, x2));
-      st_half4(kt_img + img_off(r), mul4(ys, mul4(SJ, splat4(ms.kn[i]))));
+      st_half4(kt_img + img_off(r), mul4(ys, mul4(SJ, splat4(knr[r]))));
     }
     umma::fence_proxy_async_smem();
     umma::fence_before_sync();
