@@ -1,19 +1,20 @@
 // K2: head-parallel chunk recurrence of the KDA chunked forward, on the
 // 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
-// One CTA per (sequence, head, 64-wide slice of V). The CTA walks the chunks
-// of its sequence in order and carries its K x 64 slice of the state S (the
+// One CTA per (sequence, head, BV-wide slice of V; BV = 64, or 16 when that
+// gives too few CTAs to fill the GPU). The CTA walks the chunks of its sequence
+// in order and carries its K x BV slice of the state S (the
 // FlashKDA "K2" stage, FlashKDA page, section "커널 퓨전(Kernel Fusion) 전략의
 // 분리"; the cuLA "chunk gated delta h" + "chunk fwd o" stages, cuLA launch
 // blog, section "Status & Roadmap"). Per chunk, with M = [-Tb ; P Tb] from
 // the prep kernel and the in-chunk decays measured from the chunk start:
 //
 //   D1 = M (khat Gamma)          = [-w ; P w]        (128 x K,  UMMA 128xKx64)
-//   D2 = M v                     = [-u ; P u]        (128 x 64, UMMA 128x64x64)
+//   D2 = M v                     = [-u ; P u]        (128 x BV, UMMA 128xBVx64)
 //   WQ = [w ; q~ - P w],  q~ = qhat Gamma            (fp16 operand)
-//   D2 += WQ S                   = [-U ; O]          (UMMA 128x64xK)
+//   D2 += WQ S                   = [-U ; O]          (UMMA 128xBVxK)
 //   U -> fp16, o = O -> bf16   (the output scale is folded into P and q~)
-//   D3 = k~^T U,  k~ = khat Gamma_last / Gamma       (UMMA 128x64x64)
+//   D3 = k~^T U,  k~ = khat Gamma_last / Gamma       (UMMA 128xBVx64)
 //   S  = Gamma_last S + D3                           (fp32 master in registers)
 //
 // Gamma_i is the product of the per-token decays alpha up to token i (all
