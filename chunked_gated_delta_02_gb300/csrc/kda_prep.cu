@@ -79,11 +79,11 @@ struct PrepLayout {
   static constexpr uint32_t matT = 64 * LD * 4;
   static_assert(matAt + 64 * LDQ * 4 <= matT, "A overlaps T");
   static constexpr uint32_t Z = matT + 64 * LD * 4;             // [4][16][16] fp32 merge scratch
-  static constexpr uint32_t opT = 38 * 1024;                    // Tb^T:     2 panels x  64 rows x 128 B
-  static constexpr uint32_t opM = 54 * 1024;                    // [-I ; P]: 2 panels x 128 rows x 128 B
-  static constexpr uint32_t end = opM + 2 * 128 * 128;
+  static constexpr uint32_t opT = 38 * 1024;                    // Tb^T:      64 rows x 128 B (fp16)
+  static constexpr uint32_t opM = 46 * 1024;                    // [-I ; P]: 128 rows x 128 B (fp16)
+  static constexpr uint32_t end = (opM + 128 * 128 > opEnd) ? opM + 128 * 128 : opEnd;
   static_assert(Z + 4 * 16 * 16 * 4 <= opT, "A/T/Z overlap the Tb^T operand");
-  static_assert(opT + 2 * 64 * 128 <= opM, "Tb^T operand overlaps the [-I ; P] operand");
+  static_assert(opT + 64 * 128 <= opM, "Tb^T operand overlaps the [-I ; P] operand");
   static_assert(end >= opEnd, "layout end");
 };
 
@@ -119,6 +119,11 @@ __device__ __forceinline__ F4 f4_of(float4 v) { return {make_float2(v.x, v.y), m
 __device__ __forceinline__ float4 float4_of(F4 v) { return make_float4(v.lo.x, v.lo.y, v.hi.x, v.hi.y); }
 __device__ __forceinline__ F4 bf4_to_f4(uint2 u) { return {bf2_to_f2(u.x), bf2_to_f2(u.y)}; }
 __device__ __forceinline__ uint2 ldg_u64(const __nv_bfloat16 *p) { return __ldg(reinterpret_cast<const uint2 *>(p)); }
+// two floats as an fp16 pair (round to nearest), low half first
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
 // four tf32-rounded values, one 16-byte store
 __device__ __forceinline__ void st_tf32x4(unsigned char *p, F4 v) {
   *reinterpret_cast<float4 *>(p) = make_float4(tf32_rn(v.lo.x), tf32_rn(v.lo.y), tf32_rn(v.hi.x), tf32_rn(v.hi.y));
@@ -466,30 +471,30 @@ prep_kernel(const Problem p) {
         }
         continue;
       }
-      // lower-left quarter of A (rows >= 32, columns < 32), or a P row of the [-I ; P] operand
+      // lower-left quarter of A (rows >= 32, columns < 32, fp32), or a P row of the [-I ; P]
+      // operand (fp16, 8 columns per swizzled 16-byte chunk)
       unsigned char *rowp = isA ? reinterpret_cast<unsigned char *>(&matAll[row - 32][0])
-                                : sm + Lay::opM + (uint32_t)(Jb >> 1) * (128 * 128) + (uint32_t)row * 128;
-      const int c0 = isA ? 4 * Jb : 4 * (Jb & 1);
+                                : sm + Lay::opM + (uint32_t)row * 128;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float4 knj = *reinterpret_cast<const float4 *>(&ms.kn[16 * Jb + 4 * q]);
         const float kj[4] = {knj.x, knj.y, knj.z, knj.w};
-        float4 v;
-        float *pv = &v.x;
+        float y[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float y = (16 * Jb + 4 * q + e < thr) ? x[4 * q + e] * rowf * kj[e] : 0.f;
-          pv[e] = isA ? y : tf32_rn(y);
+        for (int e = 0; e < 4; ++e) y[e] = (16 * Jb + 4 * q + e < thr) ? x[4 * q + e] * rowf * kj[e] : 0.f;
+        if (isA) {
+          *reinterpret_cast<float4 *>(rowp + ((4 * Jb + q) << 4)) = make_float4(y[0], y[1], y[2], y[3]);
+        } else {
+          const uint32_t cc = (uint32_t)(2 * Jb + (q >> 1));
+          *reinterpret_cast<uint2 *>(rowp + (((cc ^ (uint32_t)xs) << 4) | ((uint32_t)(q & 1) << 3))) =
+              make_uint2(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]));
         }
-        *reinterpret_cast<float4 *>(rowp + (((c0 + q) ^ xs) << 4)) = v;
       }
     }
   }
-  // Tb^T operand (row j, column m: T[m][j] beta_j, tf32) in 2 panels of 32 columns m: the 16-byte
-  // chunk of (row j, columns m4 .. m4 + 3)
-  auto opT_chunk = [&](int j, int m4) -> unsigned char * {
-    return sm + Lay::opT + (uint32_t)(m4 >> 5) * (64 * 128) + umma::sw128_chunk(j, (m4 & 31) >> 2);
-  };
+  // Tb^T operand (row j, column m: T[m][j] beta_j, fp16): the 16-byte chunk of (row j, columns
+  // 8 c8 .. 8 c8 + 7)
+  auto opT_chunk = [&](int j, int c8) -> unsigned char * { return sm + Lay::opT + umma::sw128_chunk(j, c8); };
   if (tid < 64) {
     // ---- pass 4a (warps 0-1): the 32 x 32 diagonal halves of T by forward substitution. Thread =
     // column col of half hh, its 32 rows in registers. Step j, with x_j final, subtracts
@@ -514,30 +519,34 @@ prep_kernel(const Problem p) {
     }
     const float bj = ms.beta[o + col];
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<float4 *>(opT_chunk(o + col, o + 4 * c)) =
-          make_float4(tf32_rn(x[4 * c] * bj), tf32_rn(x[4 * c + 1] * bj), tf32_rn(x[4 * c + 2] * bj), tf32_rn(x[4 * c + 3] * bj));
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4 *>(opT_chunk(o + col, (o >> 3) + c)) =
+          make_uint4(pack_h2(x[8 * c] * bj, x[8 * c + 1] * bj), pack_h2(x[8 * c + 2] * bj, x[8 * c + 3] * bj),
+                     pack_h2(x[8 * c + 4] * bj, x[8 * c + 5] * bj), pack_h2(x[8 * c + 6] * bj, x[8 * c + 7] * bj));
 #pragma unroll
     for (int i = 0; i < 32; ++i) matT[o + i][o + col] = x[i];
   } else {
-    // warps 2-7 meanwhile, as 16-byte stores: the -I half of [-I ; P] and the zeros above the
-    // block diagonal of P (row i, 4-column group cq), then the zero upper-right quarter of Tb^T
-    // (rows j >= 32, columns m < 32). A above its block diagonal is never read.
+    // warps 2-7 meanwhile, as 16-byte stores of 8 fp16 columns: the -I half of [-I ; P] and the
+    // zeros above the block diagonal of P (row i, chunk cc), then the zero upper-right quarter of
+    // Tb^T (rows j >= 32, columns m < 32). A above its block diagonal is never read.
+    constexpr uint32_t kHalfMinusOne = 0xBC00u;   // fp16 -1.0
 #pragma unroll 1
-    for (int x = tid - 64; x < 64 * 16 + 32 * 8; x += kPrepThreads - 64) {
-      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (x >= 64 * 16) {
-        const int y = x - 64 * 16;
-        *reinterpret_cast<float4 *>(opT_chunk(32 + (y >> 3), 4 * (y & 7))) = z;
+    for (int x = tid - 64; x < 64 * 8 + 32 * 4; x += kPrepThreads - 64) {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      if (x >= 64 * 8) {
+        const int y = x - 64 * 8;
+        *reinterpret_cast<uint4 *>(opT_chunk(32 + (y >> 2), y & 3)) = z;
         continue;
       }
-      const int i = x >> 4, cq = x & 15;
-      const bool dg = (i >> 2) == cq;   // this group holds the diagonal entry (i, i)
-      const float4 v = make_float4(dg && (i & 3) == 0 ? -1.f : 0.f, dg && (i & 3) == 1 ? -1.f : 0.f,
-                                   dg && (i & 3) == 2 ? -1.f : 0.f, dg && (i & 3) == 3 ? -1.f : 0.f);
-      unsigned char *pan = sm + Lay::opM + (uint32_t)(cq >> 3) * (128 * 128);
-      *reinterpret_cast<float4 *>(pan + umma::sw128_chunk(i, cq & 7)) = v;
-      if (cq >= 4 * ((i >> 4) + 1)) *reinterpret_cast<float4 *>(pan + umma::sw128_chunk(64 + i, cq & 7)) = z;
+      const int i = x >> 3, cc = x & 7;
+      uint4 v = z;
+      if ((i >> 3) == cc) {   // this chunk holds the diagonal entry (i, i)
+        const uint32_t w = ((i & 1) ? kHalfMinusOne << 16 : kHalfMinusOne);
+        const int word = (i & 7) >> 1;
+        v = make_uint4(word == 0 ? w : 0u, word == 1 ? w : 0u, word == 2 ? w : 0u, word == 3 ? w : 0u);
+      }
+      *reinterpret_cast<uint4 *>(sm + Lay::opM + umma::sw128_chunk(i, cc)) = v;
+      if (cc >= 2 * ((i >> 4) + 1)) *reinterpret_cast<uint4 *>(sm + Lay::opM + umma::sw128_chunk(64 + i, cc)) = z;
     }
   }
   __syncthreads();
@@ -575,12 +584,12 @@ prep_kernel(const Problem p) {
     {
       float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int c = 2; c <= a; ++c) strip(&matT[16 * a + i][16 * c], &Zs[2 * (c - 2) + b][0][c4], 16, t);
-      // T[m][j] for m = 16 a + i and j = 16 b + c4 .. + 3: element m % 4 of chunk (row j, m)
+      // T[m][j] for m = 16 a + i and j = 16 b + c4 .. + 3: element m % 8 of chunk (row j, m / 8)
       const int m = 16 * a + i, j = 16 * b + c4;
       const float tv[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        reinterpret_cast<float *>(opT_chunk(j + e, m & ~3))[m & 3] = tf32_rn(-tv[e] * ms.beta[j + e]);
+        reinterpret_cast<__half *>(opT_chunk(j + e, m >> 3))[m & 7] = __float2half_rn(-tv[e] * ms.beta[j + e]);
     }
   }
 
@@ -590,12 +599,11 @@ prep_kernel(const Problem p) {
   __syncthreads();
   if (tid == 0) {
     umma::fence_after_sync();
-    const uint32_t id = umma::idesc_tf32(128, 64, 0, 0);
+    const uint32_t id = umma::idesc_f16(128, 64, 0, 0);   // fp16 A and B, K-major
     const uint64_t a0 = umma::sdesc_sw128(sbase + Lay::opM, 16, 1024), b0 = umma::sdesc_sw128(sbase + Lay::opT, 16, 1024);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-      umma::mma_tf32_ss(tmem + 192, umma::desc_add(a0, (ks >> 2) * (128 * 128) + (ks & 3) * 32),
-                        umma::desc_add(b0, (ks >> 2) * (64 * 128) + (ks & 3) * 32), id, ks > 0);
+    for (int ks = 0; ks < 4; ++ks)
+      umma::mma_f16_ss(tmem + 192, umma::desc_add(a0, ks * 32), umma::desc_add(b0, ks * 32), id, ks > 0);
     umma::commit(&ms.bar);
   }
   wait_mma();
