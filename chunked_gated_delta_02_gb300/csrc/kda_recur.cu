@@ -91,7 +91,7 @@ struct RecTmem {
 
 // Small per-CTA state after the operand buffers. Arrays of two are per chunk parity.
 struct RecMisc {
-  uint64_t bar_in[2], bar_qt[2], bar_kt[2], bar_d12[2], bar_wq[2], bar_mma2[2], bar_mma1, bar_exit;
+  uint64_t bar_in[2], bar_qt[2], bar_kt[2], bar_d12[2], bar_wq[2], bar_mma2[2], bar_mma1[2], bar_uh, bar_exit;
   uint32_t tmem_slot;
   int err;
 };
@@ -107,6 +107,9 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   using Lay = RecLayout<K, BV>;
   using Tm = RecTmem<K, BV>;
   constexpr int CW = BV >= 32 ? 32 : 16;   // TMEM columns read per wait in the chain
+  // With 64-column slices the prep sub-group that owns chunk n, idle until D3 of chunk n is done,
+  // reads and converts U columns 32..63 of that chunk while the chain does columns 0..31.
+  constexpr bool kHelpU = (BV == 64);
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // 1024-byte aligned base, derived from the __shared__ array by pointer arithmetic so that the
   // compiler keeps every access in the shared address space
@@ -144,8 +147,9 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       umma::mbar_init(&ms.bar_d12[b], 1);
       umma::mbar_init(&ms.bar_wq[b], 1);
       umma::mbar_init(&ms.bar_mma2[b], 1);
+      umma::mbar_init(&ms.bar_mma1[b], 1);
     }
-    umma::mbar_init(&ms.bar_mma1, 1);
+    umma::mbar_init(&ms.bar_uh, kSubThreads / 2);   // the two U-lane warps of a prep sub-group
     umma::mbar_init(&ms.bar_exit, 3);   // the three threads that issue tensor-core work
     umma::mbar_fence_init();
     ms.err = 0;
@@ -245,15 +249,16 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
         const uint64_t b0 = umma::sdesc_sw128(sbase + Lay::Sh, K * 128, 1024);
 #pragma unroll
         for (int ks = 0; ks < K / 16; ++ks) umma::mma_f16_ts(tD2, tD12 + ks * 8, umma::desc_add(b0, ks * 2048), id, 1);
-        umma::commit(&ms.bar_mma1);
+        umma::commit(&ms.bar_mma1[b]);
       }
-      wait_bar(&ms.bar_mma1, (uint32_t)(n & 1));
+      wait_bar(&ms.bar_mma1[b], ph);
       // U (rows < 64) -> fp16 operand; o = O (rows >= 64, the scale is folded into P and q~) ->
       // bf16 global. D3 = k~^T U needs U complete and, since its commit releases D2 to the next
       // chunk of this parity, every D2 read done: the U warps wait at kBarE, the O warps only
       // arrive there once their last read is complete and store o after.
+      const int c_end = (kHelpU && tid < kChunk) ? 32 : BV;   // U columns past 32: the prep sub-group
 #pragma unroll 1
-      for (int c0 = 0; c0 < BV; c0 += CW) {
+      for (int c0 = 0; c0 < c_end; c0 += CW) {
         float x[CW];
         if constexpr (CW == 32) umma::tmem_ld32(tD2 + lane_base + c0, x);
         else umma::tmem_ld16(tD2 + lane_base + c0, x);
@@ -288,6 +293,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
         umma::fence_before_sync();
         umma::named_bar(kBarE, kChainThreads);
       }
+      if (kHelpU && tid == 0) wait_bar(&ms.bar_uh, (uint32_t)(n & 1));   // the sub-group's U columns
       if (tid == 0 && !bad) {   // D3 = k~^T U
         umma::fence_after_sync();
         const uint32_t id = umma::idesc_f16(128, BV, 1, 1);
@@ -334,9 +340,38 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
     __nv_bfloat16 *rvb = reinterpret_cast<__nv_bfloat16 *>(sm + Lay::rv + b * (kChunk * BV * 2));
     const unsigned char *qtb = sm + Lay::qt + b * (128 * K);
     const int row = (warp & 3) * 32 + lane;   // TMEM lane of this warp's quadrant
+    // U columns 32..63 of chunk m of this parity (the U-lane warps, after MMA1 of chunk m): fp16
+    // into the operand of D3, then an arrival the chain's D3 issue waits for. The arrival also
+    // comes after an error, so that the chain's bounded wait is only the last resort. MMA1 has a
+    // barrier per chunk parity: this sub-group has waited for the phase of chunk m - 2, and the
+    // phase of chunk m + 2 needs its own work of chunk m + 2, so the wait cannot alias.
+    auto help_u = [&](int m) {
+      if (!kHelpU || (warp & 3) >= 2) return;
+      wait_bar(&ms.bar_mma1[b], (uint32_t)((m >> 1) & 1));
+      if (!bad) {
+        float x[32];
+        umma::tmem_ld32(tD12 + K + lane_base + 32, x);
+        umma::tmem_ld_wait();
+#pragma unroll
+        for (int hc = 0; hc < 4; ++hc) {
+          uint4 w;
+          w.x = pack_half2(-x[8 * hc + 0], -x[8 * hc + 1]);
+          w.y = pack_half2(-x[8 * hc + 2], -x[8 * hc + 3]);
+          w.z = pack_half2(-x[8 * hc + 4], -x[8 * hc + 5]);
+          w.w = pack_half2(-x[8 * hc + 6], -x[8 * hc + 7]);
+          *reinterpret_cast<uint4 *>(sm + Lay::Uh + umma::sw128_chunk(row, 4 + hc)) = w;
+        }
+      }
+      umma::fence_proxy_async_smem();
+      umma::fence_before_sync();
+      umma::mbar_arrive(&ms.bar_uh);
+    };
+    int pending = -1;   // the last chunk of this sub-group whose U columns are still to be done
     for (int n = sg; n < nch; n += 2) {
       const uint32_t ph = (uint32_t)((n >> 1) & 1);
       const int L = min(kChunk, si.len - n * kChunk);
+      if (n >= 2) help_u(n - 2);
+      pending = -1;
       // -- v of chunk n -> fp16, the panel after khat Gamma (vh was last read by D12 of chunk n - 2)
       wait_bar(&ms.bar_in[b], ph);
       in_done += bad ? 0u : 1u;
@@ -424,7 +459,9 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       wait_bar(&ms.bar_kt[b], ph);   // k~ and Gamma_last of chunk n landed
       kt_done += bad ? 0u : 1u;
       if (lt == 0 && !bad) umma::mbar_arrive(&ms.bar_wq[b]);
+      pending = n;
     }
+    if (pending >= 0) help_u(pending);
   }
 
   // ---- exit: no bulk copy or tensor-core work of this CTA may be in flight past this point.
