@@ -53,8 +53,8 @@ constexpr int kRecThreads = kChainThreads + 2 * kSubThreads;
 constexpr int kBVWide = 64, kBVNarrow = 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitLimit = 4000000000LL;   // ~2 s of SM clocks per wait
-// named barrier ids (0 is __syncthreads): the chain, prep sub-groups 0 and 1, and the end of
-// the chain's D2 reads (U rows written, O rows read)
+// named barrier ids (0 is __syncthreads): the chain, prep sub-groups 0 and 1, and the chain's U
+// rows written
 constexpr int kBarChain = 1, kBarE = 4;
 __device__ __forceinline__ int sub_bar(int sg) { return 2 + sg; }
 
@@ -91,7 +91,8 @@ struct RecTmem {
 
 // Small per-CTA state after the operand buffers. Arrays of two are per chunk parity.
 struct RecMisc {
-  uint64_t bar_in[2], bar_qt[2], bar_kt[2], bar_d12[2], bar_wq[2], bar_mma2[2], bar_mma1[2], bar_uh, bar_exit;
+  uint64_t bar_in[2], bar_qt[2], bar_kt[2], bar_d12[2], bar_wq[2], bar_mma2[2], bar_mma1[2], bar_o[2], bar_uh,
+      bar_exit;
   uint32_t tmem_slot;
   int err;
 };
@@ -148,6 +149,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       umma::mbar_init(&ms.bar_wq[b], 1);
       umma::mbar_init(&ms.bar_mma2[b], 1);
       umma::mbar_init(&ms.bar_mma1[b], 1);
+      umma::mbar_init(&ms.bar_o[b], kChainThreads - kChunk);   // the chain's O-row threads
     }
     umma::mbar_init(&ms.bar_uh, kSubThreads / 2);   // the two U-lane warps of a prep sub-group
     umma::mbar_init(&ms.bar_exit, 3);   // the three threads that issue tensor-core work
@@ -253,9 +255,9 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       }
       wait_bar(&ms.bar_mma1[b], ph);
       // U (rows < 64) -> fp16 operand; o = O (rows >= 64, the scale is folded into P and q~) ->
-      // bf16 global. D3 = k~^T U needs U complete and, since its commit releases D2 to the next
-      // chunk of this parity, every D2 read done: the U warps wait at kBarE, the O warps only
-      // arrive there once their last read is complete and store o after.
+      // bf16 global. D3 = k~^T U needs U complete (the U warps meet at kBarE). The O warps' reads
+      // of D2 only have to end before D12 of chunk n + 2 overwrites it: they arrive on bar_o of
+      // this parity, which the prep sub-group waits for before that D12.
       const int c_end = (kHelpU && tid < kChunk) ? 32 : BV;   // U columns past 32: the prep sub-group
 #pragma unroll 1
       for (int c0 = 0; c0 < c_end; c0 += CW) {
@@ -265,7 +267,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
         umma::tmem_ld_wait();
         if (tid >= kChunk && c0 + CW >= BV) {
           umma::fence_before_sync();
-          umma::named_arrive(kBarE, kChainThreads);
+          umma::mbar_arrive(&ms.bar_o[b]);
         }
         if (tid < kChunk) {
 #pragma unroll
@@ -291,7 +293,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       if (tid < kChunk) {
         umma::fence_proxy_async_smem();
         umma::fence_before_sync();
-        umma::named_bar(kBarE, kChainThreads);
+        umma::named_bar(kBarE, kChunk);
       }
       if (kHelpU && tid == 0) wait_bar(&ms.bar_uh, (uint32_t)(n & 1));   // the sub-group's U columns
       if (tid == 0 && !bad) {   // D3 = k~^T U
@@ -401,7 +403,10 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       // -- D12 of chunk n overwrites the accumulators, WQ and k~ buffer of chunk n - 2: wait for D3
       //    of chunk n - 2 (after it the chain has read them all). The next phase of that barrier
       //    (chunk n) needs WQ of chunk n, so this wait cannot see the wrong phase.
-      if (n >= 2) wait_bar(&ms.bar_mma2[b], (uint32_t)(((n - 2) >> 1) & 1));
+      if (n >= 2) {
+        wait_bar(&ms.bar_mma2[b], (uint32_t)(((n - 2) >> 1) & 1));
+        wait_bar(&ms.bar_o[b], (uint32_t)(((n - 2) >> 1) & 1));   // and the chain's O rows of chunk n - 2 read
+      }
       if (lt == 0 && !bad) {
         if (n >= 2) stage_kt(n);
         umma::fence_after_sync();
