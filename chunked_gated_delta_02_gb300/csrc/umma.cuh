@@ -214,14 +214,14 @@ __device__ __forceinline__ void mbar_fence_init() {
 // One try_wait; the hardware may suspend the thread for up to `hint_ns` while
 // the phase is incomplete (it resumes as soon as the phase completes), so a
 // waiting warp does not keep taking issue slots from the working ones.
-__device__ __forceinline__ uint32_t mbar_try_wait(uint64_t *bar, uint32_t parity, uint32_t hint_ns = 20000) {
+__device__ __forceinline__ uint32_t mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok;
 }
