@@ -197,7 +197,23 @@ kda_status_t fill_problem(kda::Problem &p, const Layout &L, void *ws, const void
   p.hand_stride = (long long)L.hand_stride;
   p.mats = reinterpret_cast<__half *>(p.hand);
   p.mat_stride = p.hand_stride / 2;
-  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p.dev_status), g_kda_device_status) != cudaSuccess) {
+  static kda::PerDeviceOnce once;
+  static std::atomic<int *> status_addr[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+  const cudaError_t e = once([&](int d) {
+    int *a = nullptr;
+    const cudaError_t r = cudaGetSymbolAddress(reinterpret_cast<void **>(&a), g_kda_device_status);
+    if (r == cudaSuccess && d < 64) status_addr[d].store(a, std::memory_order_relaxed);
+    return r;
+  });
+  p.dev_status = (dev >= 0 && dev < 64) ? status_addr[dev].load(std::memory_order_relaxed) : nullptr;
+  if (e == cudaSuccess && !p.dev_status &&
+      cudaGetSymbolAddress(reinterpret_cast<void **>(&p.dev_status), g_kda_device_status) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return KDA_ERR_CUDA;
   }

@@ -13,6 +13,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "exp2_poly.cuh"
 
 namespace kda {
@@ -97,6 +99,24 @@ __device__ __forceinline__ void state_store(const Problem &p, long long i, float
   if (p.flags & kStateBf16) static_cast<__nv_bfloat16 *>(p.final_state)[i] = __float2bfloat16_rn(x);
   else static_cast<float *>(p.final_state)[i] = x;
 }
+
+// Host: per-device state set once per process. A kernel's dynamic shared-memory limit and the SM
+// count are device properties; the per-call launch path only looks them up after the first call
+// on a device. (Up to 64 devices; beyond that the calls are simply made every time.)
+struct PerDeviceOnce {
+  std::atomic<uint64_t> done{0};
+  // runs f() the first time it is called for the current device; f returns cudaSuccess on success
+  template <typename F>
+  cudaError_t operator()(F &&f) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    const cudaError_t e = f(dev);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+};
 
 struct SeqInfo {
   int b;        // batch row

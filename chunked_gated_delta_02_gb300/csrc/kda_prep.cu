@@ -638,8 +638,10 @@ template <int K, uint32_t VF>
 static cudaError_t launch_prep_t(const Problem &p, cudaStream_t stream) {
   using Lay = PrepLayout;
   const size_t smem = Lay::end + sizeof(PrepMisc) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(prep_kernel<K, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  static PerDeviceOnce attr;
+  cudaError_t e = attr([&](int) {
+    return cudaFuncSetAttribute(prep_kernel<K, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.max_chunks, (unsigned)p.H);
   prep_kernel<K, VF><<<grid, kPrepThreads, smem, stream>>>(p);

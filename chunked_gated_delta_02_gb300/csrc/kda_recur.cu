@@ -498,8 +498,10 @@ template <int K, int BV>
 static cudaError_t launch_recur_t(const Problem &p, const TmaMaps &maps, cudaStream_t stream) {
   const size_t smem = RecLayout<K, BV>::bytes;
   static_assert(sizeof(RecMisc) <= 1024, "misc block");
-  cudaError_t e = cudaFuncSetAttribute(recur_tc_kernel<K, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  static PerDeviceOnce attr;
+  cudaError_t e = attr([&](int) {
+    return cudaFuncSetAttribute(recur_tc_kernel<K, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
   if (e != cudaSuccess) return e;
   const long long grid = (long long)p.N * p.H * (p.V / BV);
   recur_tc_kernel<K, BV><<<(unsigned)grid, kRecThreads, smem, stream>>>(p, maps);
@@ -508,10 +510,27 @@ static cudaError_t launch_recur_t(const Problem &p, const TmaMaps &maps, cudaStr
 
 // V-slice width: 64 unless that leaves fewer than about 80% of the SMs with a CTA.
 int recur_slice_width(const Problem &p) {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+  static PerDeviceOnce once;
+  static std::atomic<int> sm_count[64];
+  int sms = 0;
+  const cudaError_t e = once([&](int dev) {
+    int n = 0;
+    const cudaError_t r = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (r == cudaSuccess && dev < 64) sm_count[dev].store(n, std::memory_order_relaxed);
+    sms = n;
+    return r;
+  });
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return kBVWide;
+  }
+  if (sms == 0) {   // looked up by an earlier call on this device
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) sms = sm_count[dev].load(std::memory_order_relaxed);
+    if (sms == 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return kBVWide;
+    }
   }
   const long long wide_ctas = (long long)p.N * p.H * (p.V / kBVWide);
   return (5 * wide_ctas >= 4LL * sms) ? kBVWide : kBVNarrow;
