@@ -69,21 +69,23 @@ struct PrepLayout {
   static constexpr uint32_t opA = 0;                            // [k X ; q X]: 2 panels x 128 rows x 128 B
   static constexpr uint32_t opB = opA + 2 * 128 * 128;          // J side:      2 panels x 176 rows x 128 B
   static constexpr uint32_t opEnd = opB + 2 * kOpBRows * 128;
-  // after the A/P product the operands are dead: A (its lower-left quarter [32][36] row-major and
-  // its two diagonal halves transposed, [2 x 32][36]), T (fp32 [64][68]), the merge scratch, the
-  // Tb^T operand and the [-I ; P] operand take their place
-  static constexpr int LD = 68;                                 // 68 = 4 (mod 32) words: conflict-free rows
+  // after the A/P product the operands are dead. In their place: A's two diagonal halves
+  // transposed (fp32 [2 x 32][36]), the fp16 operands of the lower-left merge (32 rows of 128-byte
+  // swizzled rows each, 32 columns used), the Tb^T operand and the [-I ; P] operand.
   static constexpr int LDQ = 36;                                // 16-byte aligned rows of 32 + 4
-  static constexpr uint32_t matAll = 0;
-  static constexpr uint32_t matAt = matAll + 32 * LDQ * 4;
-  static constexpr uint32_t matT = 64 * LD * 4;
-  static_assert(matAt + 64 * LDQ * 4 <= matT, "A overlaps T");
-  static constexpr uint32_t Z = matT + 64 * LD * 4;             // [4][16][16] fp32 merge scratch
-  static constexpr uint32_t opT = 38 * 1024;                    // Tb^T:      64 rows x 128 B (fp16)
-  static constexpr uint32_t opM = 46 * 1024;                    // [-I ; P]: 128 rows x 128 B (fp16)
+  static constexpr uint32_t matAt = 0;
+  static constexpr uint32_t opAll = 10 * 1024;                  // A_[23][01]        (A of Z = A T_[01])
+  static constexpr uint32_t opT01 = 14 * 1024;                  // T_[01]^T, K-major (B of Z)
+  static constexpr uint32_t opT23 = 18 * 1024;                  // T_[23]            (A of T_[23] Z)
+  static constexpr uint32_t opZ = 22 * 1024;                    // Z, MN-major       (B of T_[23] Z)
+  static constexpr uint32_t opT = 26 * 1024;                    // Tb^T:      64 rows x 128 B (fp16)
+  static constexpr uint32_t opM = 34 * 1024;                    // [-I ; P]: 128 rows x 128 B (fp16)
   static constexpr uint32_t end = (opM + 128 * 128 > opEnd) ? opM + 128 * 128 : opEnd;
-  static_assert(Z + 4 * 16 * 16 * 4 <= opT, "A/T/Z overlap the Tb^T operand");
+  static_assert(matAt + 64 * LDQ * 4 <= opAll, "transposed A overlaps the merge operands");
   static_assert(opT + 64 * 128 <= opM, "Tb^T operand overlaps the [-I ; P] operand");
+  // the merge's A descriptors span 128 rows: rows 32..127 are other data of this block, whose
+  // products land in tensor-memory lanes that are never read
+  static_assert(opT23 + 128 * 128 <= end && opAll + 128 * 128 <= end, "merge operand span");
   static_assert(end >= opEnd, "layout end");
 };
 
@@ -147,10 +149,7 @@ prep_kernel(const Problem p) {
   // compiler keeps every access in the shared address space
   unsigned char *sm = smem_raw + ((1024u - (umma::smem_u32(smem_raw) & 1023u)) & 1023u);
   PrepMisc &ms = *reinterpret_cast<PrepMisc *>(sm + Lay::end);
-  float (*matAll)[Lay::LDQ] = reinterpret_cast<float (*)[Lay::LDQ]>(sm + Lay::matAll);   // A[32 + r][c]
   float (*matAt)[Lay::LDQ] = reinterpret_cast<float (*)[Lay::LDQ]>(sm + Lay::matAt);     // A[32 h + c][32 h + r] at [32 h + r][c]
-  float (*matT)[Lay::LD] = reinterpret_cast<float (*)[Lay::LD]>(sm + Lay::matT);
-  float (*Zs)[16][16] = reinterpret_cast<float (*)[16][16]>(sm + Lay::Z);   // [4][16][16]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long c = blockIdx.x;
@@ -430,8 +429,8 @@ prep_kernel(const Problem p) {
   // blocks {0, 1} (quadrants 0, 2) or {2, 3} (quadrants 1, 3), which need the 16-column blocks
   // {0, 1, 4} or {2, 3, 5, 6, 8, 9, 10}; the two warps of a quadrant split them and load all of
   // theirs before one wait. A rows (< 64) go to fp32 matAt (blocks of the diagonal halves,
-  // transposed) or matAll (the lower-left quarter), times beta_i |k_i|^-1 |k_j|^-1, strictly
-  // lower; P rows to the [-I ; P] operand (times |q_i|^-1 |k_j|^-1, lower with the
+  // transposed) or to the fp16 operand of the lower-left merge (the lower-left quarter), times
+  // beta_i |k_i|^-1 |k_j|^-1, strictly lower; P rows to the [-I ; P] operand (times |q_i|^-1 |k_j|^-1, lower with the
   // diagonal, tf32).
   {
     const int row = 32 * (warp & 3) + lane, I = (row & 63) >> 4;
@@ -471,10 +470,9 @@ prep_kernel(const Problem p) {
         }
         continue;
       }
-      // lower-left quarter of A (rows >= 32, columns < 32, fp32), or a P row of the [-I ; P]
-      // operand (fp16, 8 columns per swizzled 16-byte chunk)
-      unsigned char *rowp = isA ? reinterpret_cast<unsigned char *>(&matAll[row - 32][0])
-                                : sm + Lay::opM + (uint32_t)row * 128;
+      // lower-left quarter of A (rows >= 32, columns < 32), or a P row of the [-I ; P] operand:
+      // fp16, 8 columns per swizzled 16-byte chunk
+      unsigned char *rowp = isA ? sm + Lay::opAll + (uint32_t)(row - 32) * 128 : sm + Lay::opM + (uint32_t)row * 128;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float4 knj = *reinterpret_cast<const float4 *>(&ms.kn[16 * Jb + 4 * q]);
@@ -482,13 +480,9 @@ prep_kernel(const Problem p) {
         float y[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) y[e] = (16 * Jb + 4 * q + e < thr) ? x[4 * q + e] * rowf * kj[e] : 0.f;
-        if (isA) {
-          *reinterpret_cast<float4 *>(rowp + ((4 * Jb + q) << 4)) = make_float4(y[0], y[1], y[2], y[3]);
-        } else {
-          const uint32_t cc = (uint32_t)(2 * Jb + (q >> 1));
-          *reinterpret_cast<uint2 *>(rowp + (((cc ^ (uint32_t)xs) << 4) | ((uint32_t)(q & 1) << 3))) =
-              make_uint2(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]));
-        }
+        const uint32_t cc = (uint32_t)(2 * Jb + (q >> 1));
+        *reinterpret_cast<uint2 *>(rowp + (((cc ^ (uint32_t)(row & 7)) << 4) | ((uint32_t)(q & 1) << 3))) =
+            make_uint2(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]));
       }
     }
   }
@@ -499,8 +493,9 @@ prep_kernel(const Problem p) {
     // ---- pass 4a (warps 0-1): the 32 x 32 diagonal halves of T by forward substitution. Thread =
     // column col of half hh, its 32 rows in registers. Step j, with x_j final, subtracts
     // A_ij x_j from every x_i below it: independent FMAs, column j of A read as broadcast 16-byte
-    // loads of the transposed half. The column goes to matT (read by the lower-left merge) and,
-    // times beta, to row o + col of the Tb^T operand.
+    // loads of the transposed half. The column goes, times beta, to row o + col of the Tb^T
+    // operand and, as is, to the fp16 operands of the lower-left merge (T_[01] as a K-major B,
+    // T_[23] as a K-major A).
     const int hh = tid >> 5, col = tid & 31, o = 32 * hh;
     float x[32];
 #pragma unroll
@@ -523,8 +518,17 @@ prep_kernel(const Problem p) {
       *reinterpret_cast<uint4 *>(opT_chunk(o + col, (o >> 3) + c)) =
           make_uint4(pack_h2(x[8 * c] * bj, x[8 * c + 1] * bj), pack_h2(x[8 * c + 2] * bj, x[8 * c + 3] * bj),
                      pack_h2(x[8 * c + 4] * bj, x[8 * c + 5] * bj), pack_h2(x[8 * c + 6] * bj, x[8 * c + 7] * bj));
+    if (hh == 0) {   // row col of T_[01]^T: T[i][col], i = 0..31
 #pragma unroll
-    for (int i = 0; i < 32; ++i) matT[o + i][o + col] = x[i];
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4 *>(sm + Lay::opT01 + umma::sw128_chunk(col, c)) =
+            make_uint4(pack_h2(x[8 * c], x[8 * c + 1]), pack_h2(x[8 * c + 2], x[8 * c + 3]),
+                       pack_h2(x[8 * c + 4], x[8 * c + 5]), pack_h2(x[8 * c + 6], x[8 * c + 7]));
+    } else {         // column col of T_[23]: element (row i, column col)
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        reinterpret_cast<__half *>(sm + Lay::opT23 + umma::sw128_chunk(i, col >> 3))[col & 7] = __float2half_rn(x[i]);
+    }
   } else {
     // warps 2-7 meanwhile, as 16-byte stores of 8 fp16 columns: the -I half of [-I ; P] and the
     // zeros above the block diagonal of P (row i, chunk cc), then the zero upper-right quarter of
@@ -549,48 +553,53 @@ prep_kernel(const Problem p) {
       if (cc >= 2 * ((i >> 4) + 1)) *reinterpret_cast<uint4 *>(sm + Lay::opM + umma::sw128_chunk(64 + i, cc)) = z;
     }
   }
+  umma::fence_proxy_async_smem();   // the merge operands (readback and solve) to the tensor core
+  umma::fence_before_sync();
   __syncthreads();
-  // ---- pass 4b: the lower-left 32 x 32 block of T, -T_[23] A_[23][01] T_[01], in 16 x 16 blocks
-  // (row blocks a = 2, 3; column blocks b = 0, 1): Z_ab = sum_{b <= c <= 1} A_ac T_cb, then
-  // T_ab = -sum_{2 <= c <= a} T_ac Z_cb, written times beta to the Tb^T operand. A thread computes
-  // a strip of four columns of one row of a 16 x 16 block with 16-byte loads of T and Z rows.
-  auto fma4 = [](float a, const float4 b, float4 &acc) {
-    acc.x = fmaf(a, b.x, acc.x);
-    acc.y = fmaf(a, b.y, acc.y);
-    acc.z = fmaf(a, b.z, acc.z);
-    acc.w = fmaf(a, b.w, acc.w);
-  };
-  // acc += X[xr][xc .. xc + 15] (row of a 16-column block of X) times the 16 x 4 strip of Y
-  // starting at row yr, column yc (Y with leading dimension ldy)
-  auto strip = [&](const float *xrow, const float *y, int ldy, float4 &acc) {
+  // ---- pass 4b: the lower-left 32 x 32 block of T, -T_[23] A_[23][01] T_[01], as two tensor-core
+  // products on fp16 operands with fp32 accumulators in tensor-memory columns 0..63 (free after
+  // the readback): Z = A_[23][01] T_[01], then T_[23] Z. Rows 0..31 of each product (lanes of warp
+  // 0) are the result. The result times beta goes to the Tb^T operand.
+  if (tid == 0) {
+    umma::fence_after_sync();
+    const uint32_t id = umma::idesc_f16(128, 32, 0, 0);
+    const uint64_t a0 = umma::sdesc_sw128(sbase + Lay::opAll, 16, 1024), b0 = umma::sdesc_sw128(sbase + Lay::opT01, 16, 1024);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 a = *reinterpret_cast<const float4 *>(xrow + 4 * q);
-      fma4(a.x, *reinterpret_cast<const float4 *>(y + (4 * q + 0) * ldy), acc);
-      fma4(a.y, *reinterpret_cast<const float4 *>(y + (4 * q + 1) * ldy), acc);
-      fma4(a.z, *reinterpret_cast<const float4 *>(y + (4 * q + 2) * ldy), acc);
-      fma4(a.w, *reinterpret_cast<const float4 *>(y + (4 * q + 3) * ldy), acc);
-    }
-  };
-  {
-    const int i = (tid >> 2) & 15, c4 = 4 * (tid & 3);
-    const int a = 2 + (tid >> 7), b = (tid >> 6) & 1;
-    {
-      float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c = b; c <= 1; ++c) strip(&matAll[16 * (a - 2) + i][16 * c], &matT[16 * c][16 * b + c4], Lay::LD, z);
-      *reinterpret_cast<float4 *>(&Zs[2 * (a - 2) + b][i][c4]) = z;
-    }
-    __syncthreads();
-    {
-      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c = 2; c <= a; ++c) strip(&matT[16 * a + i][16 * c], &Zs[2 * (c - 2) + b][0][c4], 16, t);
-      // T[m][j] for m = 16 a + i and j = 16 b + c4 .. + 3: element m % 8 of chunk (row j, m / 8)
-      const int m = 16 * a + i, j = 16 * b + c4;
-      const float tv[4] = {t.x, t.y, t.z, t.w};
+    for (int ks = 0; ks < 2; ++ks) umma::mma_f16_ss(tmem, umma::desc_add(a0, ks * 32), umma::desc_add(b0, ks * 32), id, ks > 0);
+    umma::commit(&ms.bar);
+  }
+  wait_mma();
+  if (warp == 0) {   // Z row = lane -> fp16 row of the MN-major B operand of T_[23] Z
+    float x[32];
+    umma::tmem_ld32(tmem, x);
+    umma::tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        reinterpret_cast<__half *>(opT_chunk(j + e, m >> 3))[m & 7] = __float2half_rn(-tv[e] * ms.beta[j + e]);
-    }
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4 *>(sm + Lay::opZ + umma::sw128_chunk(lane, c)) =
+          make_uint4(pack_h2(x[8 * c], x[8 * c + 1]), pack_h2(x[8 * c + 2], x[8 * c + 3]),
+                     pack_h2(x[8 * c + 4], x[8 * c + 5]), pack_h2(x[8 * c + 6], x[8 * c + 7]));
+  }
+  umma::fence_proxy_async_smem();
+  umma::fence_before_sync();
+  __syncthreads();
+  if (tid == 0) {
+    umma::fence_after_sync();
+    const uint32_t id = umma::idesc_f16(128, 32, 0, 1);   // B = Z, MN-major
+    const uint64_t a0 = umma::sdesc_sw128(sbase + Lay::opT23, 16, 1024), b0 = umma::sdesc_sw128(sbase + Lay::opZ, 8192, 1024);
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks)
+      umma::mma_f16_ss(tmem + 32, umma::desc_add(a0, ks * 32), umma::desc_add(b0, ks * 2048), id, ks > 0);
+    umma::commit(&ms.bar);
+  }
+  wait_mma();
+  if (warp == 0) {   // row a = lane of T_[23] Z: T[32 + a][b] beta_b = -(T_[23] Z)[a][b] beta_b
+    float x[32];
+    umma::tmem_ld32(tmem + 32, x);
+    umma::tmem_ld_wait();
+    const int m = 32 + lane;
+#pragma unroll
+    for (int b = 0; b < 32; ++b)
+      reinterpret_cast<__half *>(opT_chunk(b, m >> 3))[m & 7] = __float2half_rn(-x[b] * ms.beta[b]);
   }
 
   // ---- pass 5: M = [-I ; P] Tb on the tensor cores
