@@ -46,11 +46,12 @@
 //   D = [k X ; q X] (128 x K)  x  [k Y ; k Ys ; k Ys_0 2^{B_1} ; k Ys_1 2^{B_2} ; k Ys_0 c_30]^T
 // Columns 0-63 give the diagonal blocks, 64-127 the blocks next to the
 // diagonal, 128-175 the three blocks further out. The unit lower triangular
-// inverse T = (I + A)^{-1} is blocked, in fp32: the two 32 x 32 diagonal halves by
-// forward substitution (one thread per column), then the lower-left 32 x 32 block
-// -T_[23] A_[23][01] T_[01] as 16 x 16 block products. Both write Tb = T diag(beta)
-// straight into the operand of M = [-I ; P] Tb, a second tensor-core product
-// (128 x 64 x 64).
+// inverse T = (I + A)^{-1} is blocked: the two 32 x 32 diagonal halves by forward
+// substitution in fp32 (one thread per column), then the lower-left 32 x 32 block
+// -T_[23] A_[23][01] T_[01] as two small tensor-core products (fp16 operands, fp32
+// accumulators): Z = A_[23][01] T_[01], then T_[23] Z. All of T lands, scaled as
+// Tb = T diag(beta), in the fp16 operand of M = [-I ; P] Tb, a third tensor-core
+// product (128 x 64 x 64).
 #include <type_traits>
 
 #include "kda_common.cuh"
