@@ -14,8 +14,10 @@
 
 namespace kda {
 cudaError_t launch_varlen_schedule(const Problem &p, cudaStream_t stream);
-cudaError_t launch_prep(const Problem &p, cudaStream_t stream);
-cudaError_t launch_recur(const Problem &p, const TmaMaps &maps, int bv, cudaStream_t stream);
+// overlap: launch so that the kernel may be scheduled while the kernel ahead of it in the stream
+// (the schedule kernel, the prep kernel) is still running
+cudaError_t launch_prep(const Problem &p, cudaStream_t stream, bool overlap);
+cudaError_t launch_recur(const Problem &p, const TmaMaps &maps, int bv, cudaStream_t stream, bool overlap);
 int recur_slice_width(const Problem &p);
 }  // namespace kda
 
@@ -315,16 +317,20 @@ kda_status_t kda_fwd_ex(const void *q, const void *k, const void *v, const void 
   }
   if (st == KDA_OK) {
     NvtxRange r("kda K1 prep");
-    st = from_cuda(kda::launch_prep(p, s));
+    st = from_cuda(kda::launch_prep(p, s, cu_seqlens != nullptr));
   }
-  mark(events ? events->prep_done : nullptr);
+  // With an event recorded between them the two kernels run one after the other, so that the
+  // event splits the time between them; otherwise the recurrence kernel's launch overlaps the end
+  // of the prep kernel.
+  const bool split = events && events->prep_done;
+  mark(split ? events->prep_done : nullptr);
   kda::TmaMaps maps;
   std::memset(&maps, 0, sizeof maps);
   const int bv = kda::recur_slice_width(p);
   if (st == KDA_OK && T > 0 && !encode_token_map(&maps.v, v, V, H, T, B, bv)) st = KDA_ERR_CUDA;
   if (st == KDA_OK) {
     NvtxRange r("kda K2 recurrence");
-    st = from_cuda(kda::launch_recur(p, maps, bv, s));
+    st = from_cuda(kda::launch_recur(p, maps, bv, s, !split));
   }
   mark(events ? events->recur_done : nullptr);
   release_scratch(scr, s);
@@ -368,7 +374,7 @@ kda_status_t kda_debug_chunk_matrices(const void *q, const void *k, const void *
   p.mats = static_cast<__half *>(chunk_mats);
   p.mat_stride = 2 * kda::kChunk * kda::kChunk;
   if (st == KDA_OK && cu_seqlens) st = from_cuda(kda::launch_varlen_schedule(p, s));
-  if (st == KDA_OK) st = from_cuda(kda::launch_prep(p, s));
+  if (st == KDA_OK) st = from_cuda(kda::launch_prep(p, s, cu_seqlens != nullptr));
   release_scratch(scr, s);
   return st;
 }

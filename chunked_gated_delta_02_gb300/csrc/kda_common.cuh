@@ -118,6 +118,33 @@ struct PerDeviceOnce {
   }
 };
 
+// Programmatic dependent launch (PTX griddepcontrol). A kernel launched with `overlap` set
+// (launch_kernel below) may be scheduled before the kernel ahead of it in the stream has
+// finished, once every CTA of that kernel has called pdl_launch_dependents() or exited; it
+// must call pdl_wait(), which returns once the kernel ahead has completed and its writes are
+// visible, before it reads or writes anything that kernel touches. Without the launch
+// attribute pdl_wait() returns at once.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... Params, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, bool overlap, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+  const cudaError_t last = cudaGetLastError();
+  return e != cudaSuccess ? e : last;
+}
+
 struct SeqInfo {
   int b;        // batch row
   int t0;       // first token

@@ -155,6 +155,11 @@ prep_kernel(const Problem p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long c = blockIdx.x;
   const int h = blockIdx.y;
+  // The recurrence kernel may be scheduled once every CTA of this grid has started (its CTAs wait
+  // for this grid to finish); this grid in turn waits here for the schedule kernel, when it was
+  // launched to overlap it.
+  pdl_launch_dependents();
+  pdl_wait();
   if (p.flag && *p.flag != kDevOk) return;
   const long long total = p.cu ? (long long)p.chunk_off[p.N] : (long long)p.B * p.nc_fixed;
   if (c >= total) return;
@@ -645,7 +650,7 @@ prep_kernel(const Problem p) {
 }
 
 template <int K, uint32_t VF>
-static cudaError_t launch_prep_t(const Problem &p, cudaStream_t stream) {
+static cudaError_t launch_prep_t(const Problem &p, cudaStream_t stream, bool overlap) {
   using Lay = PrepLayout;
   const size_t smem = Lay::end + sizeof(PrepMisc) + 1024;
   static PerDeviceOnce attr;
@@ -653,29 +658,28 @@ static cudaError_t launch_prep_t(const Problem &p, cudaStream_t stream) {
     return cudaFuncSetAttribute(prep_kernel<K, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)p.max_chunks, (unsigned)p.H);
-  prep_kernel<K, VF><<<grid, kPrepThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(prep_kernel<K, VF>, dim3((unsigned)p.max_chunks, (unsigned)p.H), dim3(kPrepThreads), smem,
+                       stream, overlap, p);
 }
 
 template <int K>
-static cudaError_t launch_prep_k(const Problem &p, cudaStream_t stream) {
+static cudaError_t launch_prep_k(const Problem &p, cudaStream_t stream, bool overlap) {
   constexpr uint32_t G = kGatePerHead, B = kBetaF32, X = kExp2Poly;
   switch (p.flags & (G | B | X)) {
-    case 0: return launch_prep_t<K, 0>(p, stream);
-    case G: return launch_prep_t<K, G>(p, stream);
-    case B: return launch_prep_t<K, B>(p, stream);
-    case G | B: return launch_prep_t<K, G | B>(p, stream);
-    case X: return launch_prep_t<K, X>(p, stream);
-    case G | X: return launch_prep_t<K, G | X>(p, stream);
-    case B | X: return launch_prep_t<K, B | X>(p, stream);
-    default: return launch_prep_t<K, G | B | X>(p, stream);
+    case 0: return launch_prep_t<K, 0>(p, stream, overlap);
+    case G: return launch_prep_t<K, G>(p, stream, overlap);
+    case B: return launch_prep_t<K, B>(p, stream, overlap);
+    case G | B: return launch_prep_t<K, G | B>(p, stream, overlap);
+    case X: return launch_prep_t<K, X>(p, stream, overlap);
+    case G | X: return launch_prep_t<K, G | X>(p, stream, overlap);
+    case B | X: return launch_prep_t<K, B | X>(p, stream, overlap);
+    default: return launch_prep_t<K, G | B | X>(p, stream, overlap);
   }
 }
 
-cudaError_t launch_prep(const Problem &p, cudaStream_t stream) {
+cudaError_t launch_prep(const Problem &p, cudaStream_t stream, bool overlap) {
   if (p.max_chunks == 0) return cudaSuccess;
-  return p.K == 64 ? launch_prep_k<64>(p, stream) : launch_prep_k<128>(p, stream);
+  return p.K == 64 ? launch_prep_k<64>(p, stream, overlap) : launch_prep_k<128>(p, stream, overlap);
 }
 
 }  // namespace kda

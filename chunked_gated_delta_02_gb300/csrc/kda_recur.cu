@@ -123,6 +123,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   const int r = bid / (p.H * VT);
   const int h = (bid / VT) % p.H;
   const int v0 = (bid % VT) * BV;
+  pdl_wait();   // the prep kernel (when launched to overlap it) has finished and its writes are visible
   if (p.flag && *p.flag != kDevOk) return;
   const int s = p.cu ? p.order[r] : r;
   const SeqInfo si = seq_info(p, s);
@@ -495,7 +496,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
 }
 
 template <int K, int BV>
-static cudaError_t launch_recur_t(const Problem &p, const TmaMaps &maps, cudaStream_t stream) {
+static cudaError_t launch_recur_t(const Problem &p, const TmaMaps &maps, cudaStream_t stream, bool overlap) {
   const size_t smem = RecLayout<K, BV>::bytes;
   static_assert(sizeof(RecMisc) <= 1024, "misc block");
   static PerDeviceOnce attr;
@@ -504,8 +505,8 @@ static cudaError_t launch_recur_t(const Problem &p, const TmaMaps &maps, cudaStr
   });
   if (e != cudaSuccess) return e;
   const long long grid = (long long)p.N * p.H * (p.V / BV);
-  recur_tc_kernel<K, BV><<<(unsigned)grid, kRecThreads, smem, stream>>>(p, maps);
-  return cudaGetLastError();
+  return launch_kernel(recur_tc_kernel<K, BV>, dim3((unsigned)grid), dim3(kRecThreads), smem, stream, overlap, p,
+                       maps);
 }
 
 // V-slice width: 64 unless that leaves fewer than about 80% of the SMs with a CTA.
@@ -536,11 +537,13 @@ int recur_slice_width(const Problem &p) {
   return (5 * wide_ctas >= 4LL * sms) ? kBVWide : kBVNarrow;
 }
 
-cudaError_t launch_recur(const Problem &p, const TmaMaps &maps, int bv, cudaStream_t stream) {
+cudaError_t launch_recur(const Problem &p, const TmaMaps &maps, int bv, cudaStream_t stream, bool overlap) {
   if (p.N == 0) return cudaSuccess;
   if (bv == kBVNarrow)
-    return p.K == 64 ? launch_recur_t<64, kBVNarrow>(p, maps, stream) : launch_recur_t<128, kBVNarrow>(p, maps, stream);
-  return p.K == 64 ? launch_recur_t<64, kBVWide>(p, maps, stream) : launch_recur_t<128, kBVWide>(p, maps, stream);
+    return p.K == 64 ? launch_recur_t<64, kBVNarrow>(p, maps, stream, overlap)
+                     : launch_recur_t<128, kBVNarrow>(p, maps, stream, overlap);
+  return p.K == 64 ? launch_recur_t<64, kBVWide>(p, maps, stream, overlap)
+                   : launch_recur_t<128, kBVWide>(p, maps, stream, overlap);
 }
 
 }  // namespace kda

@@ -25,6 +25,7 @@ varlen_schedule_kernel(const int32_t *__restrict__ cu, int N, int T, int32_t *__
   __shared__ int s_bad;
   __shared__ int s_scan[kSchedThreads];
   __shared__ int s_bins[kSchedBins];
+  pdl_launch_dependents();   // the prep kernel's CTAs may take their SMs now and wait there
   const int tid = threadIdx.x;
   if (tid == 0) s_bad = (cu[0] != 0 || cu[N] != T) ? 1 : 0;
   __syncthreads();

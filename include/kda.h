@@ -162,6 +162,11 @@ KDA_API kda_status_t kda_fwd(const void *q, const void *k, const void *v, const 
  * member may be NULL. prep_start precedes the varlen schedule (if any) and
  * the prep kernel; prep_done separates the prep kernel from the recurrence
  * kernel; recur_done follows the recurrence kernel.
+ * Without prep_done the recurrence kernel is launched to overlap the end of
+ * the prep kernel (programmatic dependent launch: its blocks may take the SMs
+ * the prep kernel frees, and wait on the GPU for it to finish before they
+ * read anything), as kda_fwd() does; with prep_done it starts after the prep
+ * kernel has finished, so that the event splits the time between the two.
  */
 typedef struct {
   void *prep_start;

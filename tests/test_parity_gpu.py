@@ -91,6 +91,27 @@ def test_deterministic():
     assert torch.equal(o1, o2) and torch.equal(f1, f2)
 
 
+@pytest.mark.parametrize("w", [custom(B=2, T=257, H=3, K=128, V=128, init_state=True),
+                               custom(H=2, K=64, V=64, seqlens=[0, 1, 63, 64, 65, 150, 7])],
+                         ids=["fixed", "varlen"])
+def test_launch_modes_agree(w):
+    """The recurrence kernel launched to overlap the prep kernel (no event between them, as in
+    kda_fwd) and launched after it (an event between them) give the same bits."""
+    import chunked_gated_delta_02_gb300 as kda
+    d = to_dev(make_inputs(w, seed=12))
+    outs = []
+    for mode in ("overlap", "split", "none"):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        events = {"overlap": (ev[0], None, ev[2]), "split": tuple(ev), "none": None}[mode]
+        o, fs = kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"], d["lower_bound"],
+                        d["scale"], d["initial_state"], True, d["cu_seqlens"], events=events)
+        torch.cuda.synchronize()
+        outs.append((o, fs))
+    for o, fs in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(fs, outs[0][1])
+    assert kda.device_status() == 0
+
+
 def test_prep_stage_matrices():
     """K1 alone: M = [-T diag(b) ; P T diag(b)] against the chunkwise fp64 oracle."""
     import chunked_gated_delta_02_gb300 as kda
