@@ -431,39 +431,50 @@ prep_kernel(const Problem p) {
   // ---- pass 3: read A and P back from TMEM (cols 0..175)
   wait_mma();
   __syncthreads();
-  // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (lane = D row). A lane quadrant holds the row
-  // blocks {0, 1} (quadrants 0, 2) or {2, 3} (quadrants 1, 3), which need the 16-column blocks
-  // {0, 1, 4} or {2, 3, 5, 6, 8, 9, 10}; the two warps of a quadrant split them and load all of
-  // theirs before one wait. A rows (< 64) go to fp32 matAt (blocks of the diagonal halves,
-  // transposed) or to the fp16 operand of the lower-left merge (the lower-left quarter), times
-  // beta_i |k_i|^-1 |k_j|^-1, strictly lower; P rows to the [-I ; P] operand (times |q_i|^-1 |k_j|^-1, lower with the
-  // diagonal, tf32).
+  // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (lane = D row): the row blocks {Ilo, Ilo + 1}, with
+  // Ilo = 0 (quadrants 0, 2) or 2 (quadrants 1, 3), one per half-warp. Each step of a warp handles
+  // one block column J for both row blocks at once: it loads the D column block of (Ilo, J) and of
+  // (Ilo + 1, J) and each half-warp keeps its own. The two warps of a quadrant split the J: J = 0
+  // and 1 (none) for the first warp of an upper (lower) quadrant, J = 2 and 3 (1) for the second.
+  // A rows (< 64) go to fp32 matAt (blocks of the diagonal halves, transposed) or to the fp16
+  // operand of the lower-left merge (the lower-left quarter), times beta_i |k_i|^-1 |k_j|^-1,
+  // strictly lower; P rows to the [-I ; P] operand (times |q_i|^-1 |k_j|^-1, lower with the
+  // diagonal).
   {
-    const int row = 32 * (warp & 3) + lane, I = (row & 63) >> 4;
+    const int quad = warp & 3, row = 32 * quad + lane, I = (row & 63) >> 4;
+    const int Ilo = 2 * (quad & 1);
+    const bool hi = (lane >> 4) != 0;   // this lane's row block is Ilo + 1
     const bool isA = row < 64;
     const float rowf = isA ? ms.beta[row] * ms.kn[row] : ms.qn[row - 64] * p.scale;
     const int thr = isA ? row : row - 63;   // column j is kept when j < thr
-    const int xs = isA ? 0 : (row & 7);
-    const int sel = (warp & 1) * 2 + (warp >> 2);   // (upper row blocks, second warp of the quadrant)
-    const int cbs[4] = {sel == 0 ? 0 : sel == 1 ? 4 : sel == 2 ? 2 : 6, sel == 0 ? 1 : sel == 2 ? 3 : sel == 3 ? 8 : -1,
-                        sel == 2 ? 5 : sel == 3 ? 9 : -1, sel == 3 ? 10 : -1};
-    float xb[4][16];
+    // D column block of row block I2, block column J2 <= I2: 0-3 the diagonal, 4-7 the blocks next
+    // to it, 8 (2, 0), 9 (3, 1), 10 (3, 0)
+    auto col_block = [](int I2, int J2) { return J2 == I2 ? I2 : J2 == I2 - 1 ? 4 + J2 : (I2 == 2 ? 8 : J2 == 1 ? 9 : 10); };
+    int Js[2];
+    Js[0] = Ilo == 0 ? (warp >> 2) : 2 * (warp >> 2);
+    Js[1] = Ilo == 0 ? -1 : 2 * (warp >> 2) + 1;
+    float xlo[2][16], xhi[2][16];
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (cbs[e] >= 0) umma::tmem_ld16(tmem + ((uint32_t)(warp & 3) * 32 << 16) + cbs[e] * 16, xb[e]);
+    for (int e = 0; e < 2; ++e) {
+      const int J = Js[e];
+      if (J < 0) continue;
+      const uint32_t lane_base = (uint32_t)quad * 32 << 16;
+      if (J <= Ilo) {
+        umma::tmem_ld16(tmem + lane_base + col_block(Ilo, J) * 16, xlo[e]);
+      } else {   // no block (Ilo, J): the lower half-warp skips this step
+#pragma unroll
+        for (int t = 0; t < 16; ++t) xlo[e][t] = 0.f;
+      }
+      umma::tmem_ld16(tmem + lane_base + col_block(Ilo + 1, J) * 16, xhi[e]);
+    }
     umma::tmem_ld_wait();
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int cb = cbs[e];
-      if (cb < 0) continue;
-      const float *x = xb[e];
-      // block column Jb of D column block cb for row block I, or -1 if it is not one of row I's
-      int Jb = -1;
-      if (cb < 4) Jb = (cb == I) ? cb : -1;
-      else if (cb < 8) Jb = (cb - 4 == I - 1) ? cb - 4 : -1;
-      else if (cb == 8) Jb = (I == 2) ? 0 : -1;
-      else Jb = (I == 3) ? (cb == 9 ? 1 : 0) : -1;
-      if (Jb < 0) continue;
+    for (int e = 0; e < 2; ++e) {
+      const int Jb = Js[e];
+      if (Jb < 0 || Jb > I) continue;
+      float x[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) x[t] = hi ? xhi[e][t] : xlo[e][t];
       if (isA && (I >> 1) == (Jb >> 1)) {   // block of a diagonal half of A: transposed, scalar stores
         float *atc = &matAt[32 * (Jb >> 1) + 16 * (Jb & 1)][row & 31];
 #pragma unroll
@@ -485,7 +496,7 @@ prep_kernel(const Problem p) {
         const float kj[4] = {knj.x, knj.y, knj.z, knj.w};
         float y[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) y[e] = (16 * Jb + 4 * q + e < thr) ? x[4 * q + e] * rowf * kj[e] : 0.f;
+        for (int e2 = 0; e2 < 4; ++e2) y[e2] = (16 * Jb + 4 * q + e2 < thr) ? x[4 * q + e2] * rowf * kj[e2] : 0.f;
         const uint32_t cc = (uint32_t)(2 * Jb + (q >> 1));
         *reinterpret_cast<uint2 *>(rowp + (((cc ^ (uint32_t)(row & 7)) << 4) | ((uint32_t)(q & 1) << 3))) =
             make_uint2(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]));
