@@ -150,7 +150,7 @@ prep_kernel(const Problem p) {
   // compiler keeps every access in the shared address space
   unsigned char *sm = smem_raw + ((1024u - (umma::smem_u32(smem_raw) & 1023u)) & 1023u);
   PrepMisc &ms = *reinterpret_cast<PrepMisc *>(sm + Lay::end);
-  float (*matAt)[Lay::LDQ] = reinterpret_cast<float (*)[Lay::LDQ]>(sm + Lay::matAt);     // A[32 h + c][32 h + r] at [32 h + r][c]
+  float (*matAt)[Lay::LDQ] = reinterpret_cast<float (*)[Lay::LDQ]>(sm + Lay::matAt);     // -A[32 h + c][32 h + r] at [32 h + r][c]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long c = blockIdx.x;
@@ -436,10 +436,10 @@ prep_kernel(const Problem p) {
   // one block column J for both row blocks at once: it loads the D column block of (Ilo, J) and of
   // (Ilo + 1, J) and each half-warp keeps its own. The two warps of a quadrant split the J: J = 0
   // and 1 (none) for the first warp of an upper (lower) quadrant, J = 2 and 3 (1) for the second.
-  // A rows (< 64) go to fp32 matAt (blocks of the diagonal halves, transposed) or to the fp16
-  // operand of the lower-left merge (the lower-left quarter), times beta_i |k_i|^-1 |k_j|^-1,
-  // strictly lower; P rows to the [-I ; P] operand (times |q_i|^-1 |k_j|^-1, lower with the
-  // diagonal).
+  // A rows (< 64) go to fp32 matAt (blocks of the diagonal halves, negated and transposed) or to
+  // the fp16 operand of the lower-left merge (the lower-left quarter), times
+  // beta_i |k_i|^-1 |k_j|^-1, strictly lower; P rows to the [-I ; P] operand (times
+  // |q_i|^-1 |k_j|^-1, lower with the diagonal).
   {
     const int quad = warp & 3, row = 32 * quad + lane, I = (row & 63) >> 4;
     const int Ilo = 2 * (quad & 1);
@@ -475,15 +475,16 @@ prep_kernel(const Problem p) {
       float x[16];
 #pragma unroll
       for (int t = 0; t < 16; ++t) x[t] = hi ? xhi[e][t] : xlo[e][t];
-      if (isA && (I >> 1) == (Jb >> 1)) {   // block of a diagonal half of A: transposed, scalar stores
+      if (isA && (I >> 1) == (Jb >> 1)) {   // block of a diagonal half of -A: transposed, scalar stores
         float *atc = &matAt[32 * (Jb >> 1) + 16 * (Jb & 1)][row & 31];
+        const float nrowf = -rowf;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float4 knj = *reinterpret_cast<const float4 *>(&ms.kn[16 * Jb + 4 * q]);
           const float kj[4] = {knj.x, knj.y, knj.z, knj.w};
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2)
-            atc[(4 * q + e2) * Lay::LDQ] = (16 * Jb + 4 * q + e2 < thr) ? x[4 * q + e2] * rowf * kj[e2] : 0.f;
+            atc[(4 * q + e2) * Lay::LDQ] = (16 * Jb + 4 * q + e2 < thr) ? x[4 * q + e2] * nrowf * kj[e2] : 0.f;
         }
         continue;
       }
@@ -508,26 +509,32 @@ prep_kernel(const Problem p) {
   auto opT_chunk = [&](int j, int c8) -> unsigned char * { return sm + Lay::opT + umma::sw128_chunk(j, c8); };
   if (tid < 64) {
     // ---- pass 4a (warps 0-1): the 32 x 32 diagonal halves of T by forward substitution. Thread =
-    // column col of half hh, its 32 rows in registers. Step j, with x_j final, subtracts
-    // A_ij x_j from every x_i below it: independent FMAs, column j of A read as broadcast 16-byte
-    // loads of the transposed half. The column goes, times beta, to row o + col of the Tb^T
-    // operand and, as is, to the fp16 operands of the lower-left merge (T_[01] as a K-major B,
-    // T_[23] as a K-major A).
+    // column col of half hh, its 32 rows in registers as 16 pairs. Step j, with x_j final,
+    // adds (-A_ij) x_j to every x_i below it: independent packed FMAs on row pairs, column j of -A
+    // read as broadcast 16-byte loads of the transposed half. A pair that holds row j itself
+    // takes the coefficient -A_jj = 0, so x_j stays as it is. The column goes, times beta, to row
+    // o + col of the Tb^T operand and, as is, to the fp16 operands of the lower-left merge (T_[01]
+    // as a K-major B, T_[23] as a K-major A).
     const int hh = tid >> 5, col = tid & 31, o = 32 * hh;
-    float x[32];
+    float2 x2[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = (i == col) ? 1.f : 0.f;
+    for (int m = 0; m < 16; ++m) x2[m] = make_float2(2 * m == col ? 1.f : 0.f, 2 * m + 1 == col ? 1.f : 0.f);
 #pragma unroll
     for (int j = 0; j < 31; ++j) {
-      const float xj = x[j];
+      const float xj = (j & 1) ? x2[j >> 1].y : x2[j >> 1].x;
+      const float2 xjj = make_float2(xj, xj);
 #pragma unroll
       for (int q = (j + 1) / 4; q < 8; ++q) {
-        const float4 a = *reinterpret_cast<const float4 *>(&matAt[o + j][4 * q]);
-        if (4 * q + 0 > j) x[4 * q + 0] = fmaf(-a.x, xj, x[4 * q + 0]);
-        if (4 * q + 1 > j) x[4 * q + 1] = fmaf(-a.y, xj, x[4 * q + 1]);
-        if (4 * q + 2 > j) x[4 * q + 2] = fmaf(-a.z, xj, x[4 * q + 2]);
-        if (4 * q + 3 > j) x[4 * q + 3] = fmaf(-a.w, xj, x[4 * q + 3]);
+        const float4 na = *reinterpret_cast<const float4 *>(&matAt[o + j][4 * q]);
+        if (4 * q + 1 > j) x2[2 * q] = __ffma2_rn(make_float2(na.x, na.y), xjj, x2[2 * q]);
+        if (4 * q + 3 > j) x2[2 * q + 1] = __ffma2_rn(make_float2(na.z, na.w), xjj, x2[2 * q + 1]);
       }
+    }
+    float x[32];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      x[2 * m] = x2[m].x;
+      x[2 * m + 1] = x2[m].y;
     }
     const float bj = ms.beta[o + col];
 #pragma unroll
