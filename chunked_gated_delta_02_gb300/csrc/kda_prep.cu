@@ -49,7 +49,7 @@
 // inverse T = (I + A)^{-1} is blocked: the two 32 x 32 diagonal halves by forward
 // substitution in fp32 (one thread per column), then the lower-left 32 x 32 block
 // -T_[23] A_[23][01] T_[01] as two small tensor-core products (fp16 operands, fp32
-// accumulators): Z = A_[23][01] T_[01], then T_[23] Z. All of T lands, scaled as
+// accumulators): Z = A_[23][01] T_[01], then (T_[23] Z)^T = Z^T T_[23]^T. All of T lands, scaled as
 // Tb = T diag(beta), in the fp16 operand of M = [-I ; P] Tb, a third tensor-core
 // product (128 x 64 x 64).
 #include <type_traits>
@@ -77,16 +77,17 @@ struct PrepLayout {
   static constexpr uint32_t matAt = 0;
   static constexpr uint32_t opAll = 10 * 1024;                  // A_[23][01]        (A of Z = A T_[01])
   static constexpr uint32_t opT01 = 14 * 1024;                  // T_[01]^T, K-major (B of Z)
-  static constexpr uint32_t opT23 = 18 * 1024;                  // T_[23]            (A of T_[23] Z)
-  static constexpr uint32_t opZ = 22 * 1024;                    // Z, MN-major       (B of T_[23] Z)
+  static constexpr uint32_t opT23 = 18 * 1024;                  // T_[23]^T, MN-major (B of Z^T T_[23]^T)
+  static constexpr uint32_t opZ = 22 * 1024;                    // Z^T, MN-major      (A of Z^T T_[23]^T)
   static constexpr uint32_t opT = 26 * 1024;                    // Tb^T:      64 rows x 128 B (fp16)
   static constexpr uint32_t opM = 34 * 1024;                    // [-I ; P]: 128 rows x 128 B (fp16)
   static constexpr uint32_t end = (opM + 128 * 128 > opEnd) ? opM + 128 * 128 : opEnd;
   static_assert(matAt + 64 * LDQ * 4 <= opAll, "transposed A overlaps the merge operands");
   static_assert(opT + 64 * 128 <= opM, "Tb^T operand overlaps the [-I ; P] operand");
-  // the merge's A descriptors span 128 rows: rows 32..127 are other data of this block, whose
-  // products land in tensor-memory lanes that are never read
-  static_assert(opT23 + 128 * 128 <= end && opAll + 128 * 128 <= end, "merge operand span");
+  // the merge's A operands span 128 rows (K-major A_[23][01]: 128 rows of 128 B; MN-major Z^T: a
+  // second 64-row panel 8 KB on, 32 K rows of 128 B): rows 32..127 are other data of this block,
+  // whose products land in tensor-memory lanes that are never read
+  static_assert(opAll + 128 * 128 <= end && opZ + 8192 + 32 * 128 <= end, "merge operand span");
   static_assert(end >= opEnd, "layout end");
 };
 
@@ -542,17 +543,14 @@ prep_kernel(const Problem p) {
       *reinterpret_cast<uint4 *>(opT_chunk(o + col, (o >> 3) + c)) =
           make_uint4(pack_h2(x[8 * c] * bj, x[8 * c + 1] * bj), pack_h2(x[8 * c + 2] * bj, x[8 * c + 3] * bj),
                      pack_h2(x[8 * c + 4] * bj, x[8 * c + 5] * bj), pack_h2(x[8 * c + 6] * bj, x[8 * c + 7] * bj));
-    if (hh == 0) {   // row col of T_[01]^T: T[i][col], i = 0..31
+    // row col of T_[01]^T (K-major B of Z = A_[23][01] T_[01]) or of T_[23]^T (MN-major B of
+    // Z^T T_[23]^T): column col of the half, T[o + i][o + col], i = 0..31
+    unsigned char *tdst = sm + (hh == 0 ? Lay::opT01 : Lay::opT23);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4 *>(sm + Lay::opT01 + umma::sw128_chunk(col, c)) =
-            make_uint4(pack_h2(x[8 * c], x[8 * c + 1]), pack_h2(x[8 * c + 2], x[8 * c + 3]),
-                       pack_h2(x[8 * c + 4], x[8 * c + 5]), pack_h2(x[8 * c + 6], x[8 * c + 7]));
-    } else {         // column col of T_[23]: element (row i, column col)
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        reinterpret_cast<__half *>(sm + Lay::opT23 + umma::sw128_chunk(i, col >> 3))[col & 7] = __float2half_rn(x[i]);
-    }
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4 *>(tdst + umma::sw128_chunk(col, c)) =
+          make_uint4(pack_h2(x[8 * c], x[8 * c + 1]), pack_h2(x[8 * c + 2], x[8 * c + 3]),
+                     pack_h2(x[8 * c + 4], x[8 * c + 5]), pack_h2(x[8 * c + 6], x[8 * c + 7]));
   } else {
     // warps 2-7 meanwhile, as 16-byte stores of 8 fp16 columns: the -I half of [-I ; P] and the
     // zeros above the block diagonal of P (row i, chunk cc), then the zero upper-right quarter of
@@ -582,8 +580,9 @@ prep_kernel(const Problem p) {
   __syncthreads();
   // ---- pass 4b: the lower-left 32 x 32 block of T, -T_[23] A_[23][01] T_[01], as two tensor-core
   // products on fp16 operands with fp32 accumulators in tensor-memory columns 0..63 (free after
-  // the readback): Z = A_[23][01] T_[01], then T_[23] Z. Rows 0..31 of each product (lanes of warp
-  // 0) are the result. The result times beta goes to the Tb^T operand.
+  // the readback): Z = A_[23][01] T_[01], then (T_[23] Z)^T = Z^T T_[23]^T, whose row b is row b of
+  // the block's part of the Tb^T operand. Rows 0..31 of each product (lanes of warp 0) are the
+  // result.
   if (tid == 0) {
     umma::fence_after_sync();
     const uint32_t id = umma::idesc_f16(128, 32, 0, 0);
@@ -593,7 +592,7 @@ prep_kernel(const Problem p) {
     umma::commit(&ms.bar);
   }
   wait_mma();
-  if (warp == 0) {   // Z row = lane -> fp16 row of the MN-major B operand of T_[23] Z
+  if (warp == 0) {   // Z row = lane -> fp16 row of the MN-major A operand Z^T of Z^T T_[23]^T
     float x[32];
     umma::tmem_ld32(tmem, x);
     umma::tmem_ld_wait();
@@ -608,22 +607,24 @@ prep_kernel(const Problem p) {
   __syncthreads();
   if (tid == 0) {
     umma::fence_after_sync();
-    const uint32_t id = umma::idesc_f16(128, 32, 0, 1);   // B = Z, MN-major
-    const uint64_t a0 = umma::sdesc_sw128(sbase + Lay::opT23, 16, 1024), b0 = umma::sdesc_sw128(sbase + Lay::opZ, 8192, 1024);
+    const uint32_t id = umma::idesc_f16(128, 32, 1, 1);   // A = Z^T and B = T_[23]^T, both MN-major
+    const uint64_t a0 = umma::sdesc_sw128(sbase + Lay::opZ, 8192, 1024), b0 = umma::sdesc_sw128(sbase + Lay::opT23, 8192, 1024);
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks)
-      umma::mma_f16_ss(tmem + 32, umma::desc_add(a0, ks * 32), umma::desc_add(b0, ks * 2048), id, ks > 0);
+      umma::mma_f16_ss(tmem + 32, umma::desc_add(a0, ks * 2048), umma::desc_add(b0, ks * 2048), id, ks > 0);
     umma::commit(&ms.bar);
   }
   wait_mma();
-  if (warp == 0) {   // row a = lane of T_[23] Z: T[32 + a][b] beta_b = -(T_[23] Z)[a][b] beta_b
+  if (warp == 0) {   // row b = lane of (T_[23] Z)^T: T[32 + i][b] beta_b = -(T_[23] Z)[i][b] beta_b, Tb^T row b
     float x[32];
     umma::tmem_ld32(tmem + 32, x);
     umma::tmem_ld_wait();
-    const int m = 32 + lane;
+    const float nb = -ms.beta[lane];
 #pragma unroll
-    for (int b = 0; b < 32; ++b)
-      reinterpret_cast<__half *>(opT_chunk(b, m >> 3))[m & 7] = __float2half_rn(-x[b] * ms.beta[b]);
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4 *>(opT_chunk(lane, 4 + c)) =
+          make_uint4(pack_h2(x[8 * c] * nb, x[8 * c + 1] * nb), pack_h2(x[8 * c + 2] * nb, x[8 * c + 3] * nb),
+                     pack_h2(x[8 * c + 4] * nb, x[8 * c + 5] * nb), pack_h2(x[8 * c + 6] * nb, x[8 * c + 7] * nb));
   }
 
   // ---- pass 5: M = [-I ; P] Tb on the tensor cores
