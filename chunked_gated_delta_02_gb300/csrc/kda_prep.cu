@@ -81,6 +81,7 @@ struct PrepLayout {
   static constexpr uint32_t opZ = 22 * 1024;                    // Z^T, MN-major      (A of Z^T T_[23]^T)
   static constexpr uint32_t opT = 26 * 1024;                    // Tb^T:      64 rows x 128 B (fp16)
   static constexpr uint32_t opM = 34 * 1024;                    // [-I ; P]: 128 rows x 128 B (fp16)
+  static constexpr uint32_t mstage = 0;                         // M, staged for its bulk copy: 128 rows x 128 B
   static constexpr uint32_t end = (opM + 128 * 128 > opEnd) ? opM + 128 * 128 : opEnd;
   static_assert(matAt + 64 * LDQ * 4 <= opAll, "transposed A overlaps the merge operands");
   static_assert(opT + 64 * 128 <= opM, "Tb^T operand overlaps the [-I ; P] operand");
@@ -89,6 +90,7 @@ struct PrepLayout {
   // whose products land in tensor-memory lanes that are never read
   static_assert(opAll + 128 * 128 <= end && opZ + 8192 + 32 * 128 <= end, "merge operand span");
   static_assert(end >= opEnd, "layout end");
+  static_assert(mstage + 128 * 128 <= opT, "the M staging copy overlaps the M product's operands");
 };
 
 struct PrepMisc {
@@ -641,30 +643,36 @@ prep_kernel(const Problem p) {
     umma::commit(&ms.bar);
   }
   wait_mma();
-  // output: row r of M (TMEM lane r) -> fp16, written in the swizzled chunk order r*8 + (cc ^ (r & 7));
-  // warp w takes lanes 32 (w % 4) .. + 31 and columns 32 (w / 4) .. + 31
+  // output: row r of M (TMEM lane r) -> fp16 row r in the swizzled chunk order r*8 + (cc ^ (r & 7)),
+  // staged in shared memory (the operands are dead) and written to the hand-off block with one
+  // bulk copy; warp w takes lanes 32 (w % 4) .. + 31 and columns 32 (w / 4) .. + 31
   {
     const int r = 32 * (warp & 3) + lane;
-    uint4 *dst = reinterpret_cast<uint4 *>(p.mats + slot * p.mat_stride) + r * 8;
+    uint4 *stage = reinterpret_cast<uint4 *>(sm + Lay::mstage) + r * 8;
 #pragma unroll 1
     for (int c0 = 32 * (warp >> 2); c0 < 32 * (warp >> 2) + 32; c0 += 16) {
       float x[16];
       umma::tmem_ld16(tmem + 192 + ((uint32_t)(warp & 3) * 32 << 16) + c0, x);
       umma::tmem_ld_wait();
-      if (ms.err) continue;
 #pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        const int cc = (c0 >> 3) + hc;
-        __half2 hv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) hv[e] = __floats2half2_rn(x[8 * hc + 2 * e], x[8 * hc + 2 * e + 1]);
-        dst[cc ^ (r & 7)] = *reinterpret_cast<const uint4 *>(hv);
-      }
+      for (int hc = 0; hc < 2; ++hc)
+        stage[((c0 >> 3) + hc) ^ (r & 7)] =
+            make_uint4(pack_h2(x[8 * hc], x[8 * hc + 1]), pack_h2(x[8 * hc + 2], x[8 * hc + 3]),
+                       pack_h2(x[8 * hc + 4], x[8 * hc + 5]), pack_h2(x[8 * hc + 6], x[8 * hc + 7]));
     }
   }
+  umma::fence_proxy_async_smem();   // the staged rows to the bulk copy
   umma::fence_before_sync();
   __syncthreads();
-  if (ms.err && tid == 0) atomicExch(p.dev_status, kDevWaitTimeout);
+  if (tid == 0) {
+    if (ms.err) {
+      atomicExch(p.dev_status, kDevWaitTimeout);
+    } else {
+      umma::bulk_s2g(p.mats + slot * p.mat_stride, sm + Lay::mstage, 128 * 128);
+      umma::bulk_commit();
+      umma::bulk_wait_read();   // the staging copy stays valid until it has been read
+    }
+  }
   if (warp == 0) umma::tmem_dealloc(tmem, kPrepTmemCols);
 }
 
