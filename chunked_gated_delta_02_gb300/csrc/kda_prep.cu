@@ -1,6 +1,6 @@
 // K1: token-parallel prep kernel of the KDA chunked forward.
 //
-// One CTA per (chunk of 64 tokens, head), two CTAs per SM. It does the work of
+// One CTA per (chunk of 64 tokens, head), heads fastest, two CTAs per SM. It does the work of
 // the FlashKDA "K1" stage (FlashKDA page, section "커널 퓨전(Kernel Fusion)
 // 전략의 분리": gate activation, L2 normalisation, decay and the triangular
 // inverse, all parallel over tokens) and the cuLA "kda chunk intra" stage
@@ -156,8 +156,9 @@ prep_kernel(const Problem p) {
   float (*matAt)[Lay::LDQ] = reinterpret_cast<float (*)[Lay::LDQ]>(sm + Lay::matAt);     // -A[32 h + c][32 h + r] at [32 h + r][c]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const long long c = blockIdx.x;
-  const int h = blockIdx.y;
+  // block = chunk * H + head: the blocks of one wave take whole token rows across the heads
+  const long long c = blockIdx.x / (unsigned)p.H;
+  const int h = (int)(blockIdx.x - c * p.H);
   // The recurrence kernel may be scheduled once every CTA of this grid has started (its CTAs wait
   // for this grid to finish); this grid in turn waits here for the schedule kernel, when it was
   // launched to overlap it.
@@ -685,8 +686,8 @@ static cudaError_t launch_prep_t(const Problem &p, cudaStream_t stream, bool ove
     return cudaFuncSetAttribute(prep_kernel<K, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
   if (e != cudaSuccess) return e;
-  return launch_kernel(prep_kernel<K, VF>, dim3((unsigned)p.max_chunks, (unsigned)p.H), dim3(kPrepThreads), smem,
-                       stream, overlap, p);
+  return launch_kernel(prep_kernel<K, VF>, dim3((unsigned)(p.max_chunks * p.H)), dim3(kPrepThreads), smem, stream,
+                       overlap, p);
 }
 
 template <int K>
