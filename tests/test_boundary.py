@@ -139,3 +139,16 @@ def test_fwd_ex_variant_alignment_rules(lib):
         assert _call_ex(lib, flags, K=96) == 2          # unsupported head dim
         assert _call_ex(lib, flags, lb=-6.0) == 1       # lower bound out of range
         assert _call_ex(lib, flags, init=FAKE + 8) == 1  # state alignment
+
+
+def test_python_binding_has_no_cpu_path(lib):
+    """The binding refuses host tensors instead of computing on the CPU: every step runs in the
+    CUDA kernels, and there is no fallback."""
+    import torch
+    import chunked_gated_delta_02_gb300 as kda
+    B, T, H, K = 1, 64, 1, 64
+    q = torch.zeros(B, T, H, K, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        kda.fwd(q, q, q, q, torch.zeros(B, T, H, dtype=torch.bfloat16), torch.zeros(H), None, -5.0)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        kda.fwd_noalloc(q, q, q, q, torch.zeros(B, T, H, dtype=torch.bfloat16), torch.zeros(H), out=q)
