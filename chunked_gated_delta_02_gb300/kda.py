@@ -84,7 +84,10 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
     instead of the SFU exponential (an implementation option, KDA_EXP2_POLY).
     Returns (o bf16 [B,T,H,V], final_state in the state layout and dtype, or None).
     events: optional (prep_start, prep_done, recur_done) torch.cuda.Event triple
-    recorded on the current stream at the kernel boundaries (profiling only).
+    recorded on the current stream at the kernel boundaries (profiling only; a None
+    entry is not recorded). Without prep_done the recurrence kernel's launch
+    overlaps the end of the prep kernel, as without events; with it the two run
+    one after the other, so that the event splits their times.
     """
     B, T, H, K = q.shape
     V = v.shape[-1]
