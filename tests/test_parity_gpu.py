@@ -112,6 +112,53 @@ def test_launch_modes_agree(w):
     assert kda.device_status() == 0
 
 
+@pytest.mark.parametrize("w", [custom(B=2, T=200, H=3, K=128, V=128, init_state=True),
+                               custom(H=2, K=64, V=64, seqlens=[0, 1, 63, 64, 65, 150, 7])],
+                         ids=["fixed", "varlen"])
+def test_cuda_graph_capture_and_replay(w):
+    """The forward captured in a CUDA graph (with a caller workspace; the kernels' overlapped
+    launches become graph edges) and replayed gives the same bits as the eager call, also
+    after new inputs are copied into the captured buffers."""
+    import chunked_gated_delta_02_gb300 as kda
+    d = to_dev(make_inputs(w, seed=13))
+    d2 = to_dev(make_inputs(w, seed=14))
+    B, T, H, K = d["q"].shape
+    V = d["v"].shape[-1]
+    N = B if d["cu_seqlens"] is None else d["cu_seqlens"].numel() - 1
+    ws = torch.empty(max(kda.workspace_size(B, T, H, K, V, N), 1), dtype=torch.uint8, device="cuda")
+    o = torch.empty(B, T, H, V, dtype=torch.bfloat16, device="cuda")
+    fs = torch.empty(N, H, V, K, dtype=torch.float32, device="cuda")
+
+    def call(x, out=None, final=None):
+        return kda.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["A_log"], x["dt_bias"], x["lower_bound"],
+                       x["scale"], x["initial_state"], True, x["cu_seqlens"], workspace=ws, out=out,
+                       final_state=final)
+
+    ref1 = [t.clone() for t in call(d)]
+    ref2 = [t.clone() for t in call(d2)]
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call(d, o, fs)   # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call(d, o, fs)
+    o.zero_()
+    fs.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref1[0]) and torch.equal(fs, ref1[1])
+    for name in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state"):
+        if d[name] is not None:
+            d[name].copy_(d2[name])
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref2[0]) and torch.equal(fs, ref2[1])
+    assert kda.device_status() == 0
+
+
 def test_prep_stage_matrices():
     """K1 alone: M = [-T diag(b) ; P T diag(b)] against the chunkwise fp64 oracle."""
     import chunked_gated_delta_02_gb300 as kda
