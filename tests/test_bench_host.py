@@ -75,3 +75,25 @@ def test_algorithmic_bytes_fixed_workload():
     th = 2 * 2048 * 32
     assert bench.algorithmic_bytes(inp, with_state=False) == th * 1282
     assert bench.algorithmic_bytes(inp) == th * 1282 + 2 * 32 * 128 * 128 * 4
+
+
+def test_reference_arm_json_line(monkeypatch):
+    """The reference arm's line (rank 0, one process): the oracle timed on the host cores, with the
+    keys the driver reads. The sample is shortened for the test."""
+    import json
+    orig = bench.cpu_baseline
+    monkeypatch.setattr(bench, "cpu_baseline", lambda inp, target_s=8.0: orig(inp, target_s=0.2))
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    args = type("A", (), {"workload": "tiny", "seed": 0, "steps": 1, "warmup": 0})()
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_reference(args)
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["value"] > 0 and line["higher_is_better"] is True and line["steps"] == 1
+    assert line["config"]["workload"].startswith("tiny")
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
