@@ -56,7 +56,28 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cp", default="auto",
+                    help="context parallelism: auto (the library's plan), off, or a segment count")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="override the workload's head count (same shapes and distributions otherwise)")
     return ap.parse_args()
+
+
+def cp_arg(text):
+    """The --cp argument as kda.fwd's context_parallel: None (auto), False (off) or a count."""
+    if text == "auto":
+        return None
+    if text == "off":
+        return False
+    return int(text)
+
+
+def workload_of(args):
+    from dataclasses import replace
+    from chunked_gated_delta_02_gb300.workloads import named
+    w = named(args.workload)
+    heads = getattr(args, "heads", None)
+    return replace(w, H=heads) if heads else w
 
 
 # --------------------------------------------------------------------------- helpers
@@ -98,19 +119,36 @@ def whole_job_rate(units_per_rank, world_size, ms_max):
     return units_per_rank * world_size / (ms_max * 1e-3)
 
 
-def kernel_rooflines(inp, ms_prep, ms_rec, peak, peak_src, workload):
-    """HBM roofline of each kernel: the algorithmic bytes of the launch over its measured time.
+def kernel_algorithmic_bytes(inp):
+    """Bytes each kernel must move by itself, per launch.
 
-    The prep kernel is credited with the token bytes (1282 B per token-head at K = V = 128), the
-    recurrence kernel with the token bytes plus the state. The dominant kernel (longer time) comes
-    first."""
+    The prep kernel (K1) must read q, k, g and beta: 3K bf16 values and one bf16 beta per
+    token-head (770 B at K = 128). The recurrence kernel (K2) must read v and write o (2V bf16
+    values per token-head, 512 B at V = 128) and read / write the state (V K fp32 values per
+    (sequence, head) and direction). The two add up to the whole path's algorithmic bytes; what
+    K1 hands K2 through the workspace is not algorithmic and is not credited to either."""
+    B, T, H, K, V, N = (inp[x] for x in ("B", "T", "H", "K", "V", "N"))
+    th = B * T * H
+    state = N * H * V * K * 4
+    prep = th * (3 * K * 2 + 2)
+    rec = th * (2 * V * 2) + state * (1 if inp["initial_state"] is not None else 0) + state
+    assert prep + rec == algorithmic_bytes(inp)
+    return {"prep": prep, "recurrence": rec}
+
+
+def kernel_rooflines(inp, ms_prep, ms_rec, peak, peak_src, workload):
+    """HBM roofline of each kernel: its own algorithmic bytes per launch over its measured time,
+    with the ncu DRAM traffic of the same kernel when the committed capture matches the current
+    sources. The dominant kernel (longer time) comes first."""
+    ab = kernel_algorithmic_bytes(inp)
     out = []
-    for name, key, ms, ab in (("prep (K1)", "prep", ms_prep, algorithmic_bytes(inp, with_state=False)),
-                              ("recurrence (K2)", "recurrence", ms_rec, algorithmic_bytes(inp))):
-        gbs = ab / (ms * 1e-3) / 1e9
+    for name, key, ms in (("prep (K1)", "prep", ms_prep), ("recurrence (K2)", "recurrence", ms_rec)):
+        gbs = ab[key] / (ms * 1e-3) / 1e9
+        tr = ncu_traffic(workload, key)
         out.append({"bound": "hbm", "kernel": name, "achieved": gbs, "peak": peak, "unit": "GB/s",
-                    "frac": gbs / peak, "traffic": ncu_traffic(workload, key),
-                    "algorithmic_bytes_per_launch": ab, "ms_per_launch": ms, "peak_source": peak_src})
+                    "frac": gbs / peak, "traffic": tr,
+                    "traffic_over_algorithmic": (tr / ab[key]) if tr else None,
+                    "algorithmic_bytes_per_launch": ab[key], "ms_per_launch": ms, "peak_source": peak_src})
     out.sort(key=lambda r: -r["ms_per_launch"])
     return out
 
@@ -119,9 +157,9 @@ def tokens_of(inp) -> int:
     return inp["B"] * inp["T"]
 
 
-def workload_desc(name, inp):
+def workload_desc(name, inp, w=None):
     from chunked_gated_delta_02_gb300.workloads import named
-    w = named(name)
+    w = w or named(name)
     return {"workload": f"{name} KDA fwd: {w.describe()}", "B": inp["B"], "T": inp["T"], "H": inp["H"],
             "K": inp["K"], "V": inp["V"], "num_seqs": inp["N"], "lower_bound": inp["lower_bound"],
             "tokens_per_step": tokens_of(inp), "token_heads_per_step": tokens_of(inp) * inp["H"],
@@ -268,8 +306,9 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    from chunked_gated_delta_02_gb300.workloads import make_inputs, named
-    inp = make_inputs(named(args.workload), seed=args.seed)
+    from chunked_gated_delta_02_gb300.workloads import make_inputs
+    w = workload_of(args)
+    inp = make_inputs(w, seed=args.seed)
     vals = []
     per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
     last = None
@@ -282,7 +321,7 @@ def run_reference(args):
            "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": tokens_of(inp) / v * 1e3 if v else None, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": workload_desc(args.workload, inp),
+           "config": workload_desc(args.workload, inp, w),
            "cpu_baseline": {"value": v, "unit": UNIT, "cores": last["cores"], "kind": "oracle",
                             "sample": last["sample"]},
            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -299,13 +338,18 @@ def run_ours(args):
     dev = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(dev)
     import chunked_gated_delta_02_gb300 as kda
-    from chunked_gated_delta_02_gb300.workloads import make_inputs, named
-    inp = make_inputs(named(args.workload), seed=args.seed + rank)
+    from chunked_gated_delta_02_gb300.workloads import make_inputs
+    w = workload_of(args)
+    inp = make_inputs(w, seed=args.seed + rank)
+    cp = cp_arg(args.cp)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     B, T, H, K, V, N = (inp[x] for x in ("B", "T", "H", "K", "V", "N"))
     o = torch.empty(B, T, H, V, dtype=torch.bfloat16, device=dev)
     fs = torch.empty(N, H, V, K, dtype=torch.float32, device=dev)
-    wsb = torch.empty(kda.workspace_size(B, T, H, K, V, N), dtype=torch.uint8, device=dev)
+    varlen = inp["cu_seqlens"] is not None
+    wsb = torch.empty(kda.workspace_size(B, T, H, K, V, N, varlen, kda.kda._cp_flags(cp)), dtype=torch.uint8,
+                      device=dev)
+    n_seg, slice_w = kda.plan(B, T, H, K, V, N, varlen, cp)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     split_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
@@ -317,7 +361,7 @@ def run_ours(args):
     def step(events):
         kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"], d["lower_bound"],
                 d["scale"], d["initial_state"], True, d["cu_seqlens"], workspace=wsb, out=o, final_state=fs,
-                events=events)
+                events=events, context_parallel=cp)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -352,20 +396,32 @@ def run_ours(args):
     ms_rec = statistics.mean(rec)
     ms_prep = statistics.mean(prep)
     ms, ms_rec, ms_prep = max_over_ranks([ms, ms_rec, ms_prep], dev)
-    e2e = None if args.no_e2e else run_e2e(args, inp, dev, kda, o, fs, wsb)
+    e2e = None if args.no_e2e else run_e2e(args, inp, dev, kda, o, fs, wsb, cp)
     if rank == 0:
         peak, peak_src = measured_peak()
         abytes = algorithmic_bytes(inp)
         path_gbs = abytes / (ms * 1e-3) / 1e9
-        roofs = kernel_rooflines(inp, ms_prep, ms_rec, peak, peak_src, args.workload)
-        kernels_per_step = 2 + (1 if inp["cu_seqlens"] is not None else 0)
+        # the committed ncu traffic is per named workload in its default plan
+        traffic_key = args.workload if (not args.heads and n_seg < 2) else f"{args.workload}-H{H}-cp{n_seg}"
+        roofs = kernel_rooflines(inp, ms_prep, ms_rec, peak, peak_src, traffic_key)
+        if n_seg >= 2:
+            roofs = [dict(r, kernel="recurrence (K2: local pass, combine, final pass)")
+                     if r["kernel"].startswith("recurrence") else r for r in roofs]
+        trs = [r["traffic"] for r in roofs]
+        path_traffic = sum(trs) if all(t is not None for t in trs) else None
+        kernels_per_step = (2 if n_seg >= 2 else 0) + 2 + (1 if inp["cu_seqlens"] is not None else 0)
         out = {"metric": METRIC, "value": whole_job_rate(tokens_of(inp), ws, ms), "unit": UNIT, "impl": "ours",
                "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-               "data": "synthetic", "config": workload_desc(args.workload, inp),
+               "data": "synthetic",
+               "config": dict(workload_desc(args.workload, inp, w),
+                              recurrence={"context_parallel_segments": n_seg, "v_slice_width": slice_w,
+                                          "cp_arg": args.cp}),
                "roofline": roofs[0], "roofline_other_kernel": roofs[1],
                "path_roofline": {"achieved": path_gbs, "frac": path_gbs / peak, "unit": "GB/s",
-                                 "algorithmic_bytes_per_step": abytes,
+                                 "peak": peak, "algorithmic_bytes_per_step": abytes,
+                                 "traffic": path_traffic,
+                                 "traffic_over_algorithmic": (path_traffic / abytes) if path_traffic else None,
                                  "ms_prep": ms_prep, "ms_recurrence": ms_rec,
                                  "split": "per-kernel times from a second run of the same steps with an "
                                           "event between the kernels"},
@@ -382,7 +438,7 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def run_e2e(args, inp, dev, kda, o, fs, wsb):
+def run_e2e(args, inp, dev, kda, o, fs, wsb, cp=None):
     """The same metric through the public API with host buffers: every step copies all of its inputs
     from pinned host memory to the device and o and final_state back, inside the timed region.
 
@@ -409,7 +465,7 @@ def run_e2e(args, inp, dev, kda, o, fs, wsb):
         d = dbufs[b]
         kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"], d["lower_bound"],
                 d["scale"], d["initial_state"], True, d["cu_seqlens"], workspace=wsb, out=outs[b][0],
-                final_state=outs[b][1])
+                final_state=outs[b][1], context_parallel=cp)
 
     def step(i, serial):
         b = 0 if serial else i & 1

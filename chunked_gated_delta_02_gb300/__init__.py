@@ -5,6 +5,7 @@ include/kda.h); this package is its thin Python binding plus the seeded
 synthetic workloads. Importing the package does not load the library: the
 first call does, and fails loudly if libkda.so has not been built.
 """
-from .kda import fwd, fwd_noalloc, NOALLOC_MAX_SCRATCH, workspace_size, debug_chunk_matrices, device_status, max_chunks  # noqa: F401
+from .kda import (fwd, fwd_noalloc, NOALLOC_MAX_SCRATCH, workspace_size, debug_chunk_matrices, device_status,  # noqa: F401
+                  max_chunks, plan, CP_OFF, CP_SEGMENTS)
 
 __version__ = "0.1.0"

@@ -25,6 +25,7 @@ STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "K
 # name -> (restype, argtypes)
 SIGNATURES = {
     "kda_fwd_workspace_size": (ctypes.c_size_t, [I, I, I, I, I, I]),
+    "kda_fwd_workspace_size_ex": (ctypes.c_size_t, [I, I, I, I, I, I, I, ctypes.c_uint32]),
     "kda_fwd": (I, [P, P, P, P, P, P, P, F, F, P, P, P, I, I, I, I, I, I, P, P, ctypes.c_size_t, P]),
     "kda_fwd_with_events": (I, [P, P, P, P, P, P, P, F, F, P, P, P, I, I, I, I, I, I, P, P, ctypes.c_size_t, P,
                                  P]),
@@ -33,6 +34,7 @@ SIGNATURES = {
     "kda_fwd_noalloc": (I, [P, P, P, P, P, P, P, F, F, P, P, P, I, I, I, I, I, I, P, P]),
     "kda_debug_chunk_matrices": (I, [P, P, P, P, P, P, F, P, I, I, I, I, I, P, P, ctypes.c_size_t, P]),
     "kda_max_chunks": (ctypes.c_int64, [I, I, I]),
+    "kda_fwd_plan": (I, [I, I, I, I, I, I, I, ctypes.c_uint32, ctypes.POINTER(I), ctypes.POINTER(I)]),
     "kda_status_string": (ctypes.c_char_p, [I]),
     "kda_get_device_status": (I, [P, ctypes.POINTER(ctypes.c_int)]),
     "kda_debug_wait_timeout": (I, [ctypes.c_longlong, P]),

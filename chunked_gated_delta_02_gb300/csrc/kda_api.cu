@@ -18,7 +18,14 @@ cudaError_t launch_varlen_schedule(const Problem &p, cudaStream_t stream);
 // (the schedule kernel, the prep kernel) is still running
 cudaError_t launch_prep(const Problem &p, cudaStream_t stream, bool overlap);
 cudaError_t launch_recur(const Problem &p, const TmaMaps &maps, int bv, cudaStream_t stream, bool overlap);
+cudaError_t launch_recur_segments(const Problem &p, const TmaMaps &maps, int pass, cudaStream_t stream,
+                                  bool overlap);
+cudaError_t launch_cp_combine(const Problem &p, cudaStream_t stream);
 int recur_slice_width(const Problem &p);
+int slice_width_for(long long N, int H, int V, int sms);
+int device_sm_count();
+int cp_max_segments(int T, int H, int V, int N, bool varlen, uint32_t cp_flags);
+int cp_auto_segments(int T, int H, int K, int V, int N, int sms, int n_max, int plain_bv);
 }  // namespace kda
 
 // Sticky per-device data-error word (KDA_DEVICE_* codes).
@@ -49,7 +56,8 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t flag_off, chunk_off_off, order_off, hand_off, hand_stride, total;
+  size_t flag_off, chunk_off_off, order_off, hand_off, hand_stride, seg_state_off, seg_start_off, total;
+  int n_seg_max;   // segments the context-parallel buffers hold (0: none)
 };
 
 bool sizes_ok(int B, int T, int H, int K, int V, int N) {
@@ -60,7 +68,7 @@ int64_t max_chunks_of(int B, int T, int N) {
   return (int64_t)B * ((T + kda::kChunk - 1) / kda::kChunk) + (int64_t)N;
 }
 
-Layout layout_of(int B, int T, int H, int K, int N) {
+Layout layout_of(int B, int T, int H, int K, int V, int N, int n_seg_max) {
   Layout L;
   size_t off = 0;
   L.flag_off = off;
@@ -73,6 +81,12 @@ Layout layout_of(int B, int T, int H, int K, int N) {
   L.hand_off = off;
   L.hand_stride = (size_t)kda::hand_bytes(K);
   off = align_up(off + ch * L.hand_stride);
+  L.n_seg_max = n_seg_max;
+  const size_t seg_blocks = (size_t)N * (size_t)(n_seg_max > 1 ? n_seg_max : 0) * (size_t)H;
+  L.seg_state_off = off;
+  off = align_up(off + seg_blocks * (size_t)(V + K) * K * sizeof(float));
+  L.seg_start_off = off;
+  off = align_up(off + seg_blocks * (size_t)V * K * sizeof(float));
   L.total = off;
   return L;
 }
@@ -112,18 +126,36 @@ bool encode_token_map(CUtensorMap *m, const void *base, int D, int H, int T, int
 
 kda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
+// Segments per sequence of context parallelism (0: the plain recurrence): forced by
+// KDA_CP_SEGMENTS, or where the host plan (kda_cp.cu) estimates a clear gain on this device.
+int cp_segments_of(int n_seg_max, uint32_t flags, int T, int H, int K, int V, int N, int plain_bv) {
+  if (n_seg_max < 2) return 0;
+  if ((flags >> kda::kCpSegShift) & 0xFFu) return n_seg_max;
+  return kda::cp_auto_segments(T, H, K, V, N, kda::device_sm_count(), n_seg_max, plain_bv);
+}
+
 static_assert(KDA_GATE_PER_HEAD == kda::kGatePerHead && KDA_BETA_F32 == kda::kBetaF32 &&
                   KDA_STATE_BF16 == kda::kStateBf16 && KDA_STATE_KV == kda::kStateKV &&
                   KDA_EXP2_POLY == kda::kExp2Poly,
               "variant flags of include/kda.h and the kernels");
-constexpr uint32_t kAllFlags = KDA_GATE_PER_HEAD | KDA_BETA_F32 | KDA_STATE_BF16 | KDA_STATE_KV | KDA_EXP2_POLY;
+static_assert(KDA_CP_OFF == kda::kCpOff && KDA_CP_SEGMENTS(3) == (3u << kda::kCpSegShift),
+              "context-parallel flags of include/kda.h and the kernels");
+constexpr uint32_t kAllFlags = KDA_GATE_PER_HEAD | KDA_BETA_F32 | KDA_STATE_BF16 | KDA_STATE_KV | KDA_EXP2_POLY |
+                               KDA_CP_OFF | KDA_CP_SEGMENTS(0xFFu);
+
+// Context-parallel part of the flags: at most one of KDA_CP_OFF and KDA_CP_SEGMENTS(n), n in [2, 64].
+bool cp_flags_ok(uint32_t flags) {
+  const uint32_t n = (flags >> kda::kCpSegShift) & 0xFFu;
+  if (n == 0) return true;
+  return !(flags & KDA_CP_OFF) && n >= 2 && n <= 64;
+}
 
 // Shared argument checks of kda_fwd_ex and kda_debug_chunk_matrices.
 kda_status_t check_common(const void *q, const void *k, const void *g, const void *beta,
                           const float *A_log, const float *dt_bias, float lower_bound,
                           const int32_t *cu_seqlens, int B, int T, int H, int K, int num_seqs,
                           uint32_t flags) {
-  if (flags & ~kAllFlags) return KDA_ERR_INVALID_ARG;
+  if ((flags & ~kAllFlags) || !cp_flags_ok(flags)) return KDA_ERR_INVALID_ARG;
   if (!sizes_ok(B, T, H, K, K, num_seqs)) return KDA_ERR_INVALID_ARG;
   // token tensors may be null only when they hold no elements (T == 0)
   if (!A_log || (T > 0 && (!q || !k || !g || !beta))) return KDA_ERR_INVALID_ARG;
@@ -197,6 +229,9 @@ kda_status_t fill_problem(kda::Problem &p, const Layout &L, void *ws, const void
   p.order = reinterpret_cast<int32_t *>(base + L.order_off);
   p.hand = reinterpret_cast<unsigned char *>(base + L.hand_off);
   p.hand_stride = (long long)L.hand_stride;
+  p.seg_state = reinterpret_cast<float *>(base + L.seg_state_off);
+  p.seg_start = reinterpret_cast<float *>(base + L.seg_start_off);
+  p.n_seg = 0;
   p.mats = reinterpret_cast<__half *>(p.hand);
   p.mat_stride = p.hand_stride / 2;
   static kda::PerDeviceOnce once;
@@ -243,9 +278,14 @@ int64_t kda_max_chunks(int B, int T, int num_seqs) {
   return max_chunks_of(B, T, num_seqs);
 }
 
+size_t kda_fwd_workspace_size_ex(int B, int T, int H, int K, int V, int num_seqs, int varlen, uint32_t flags) {
+  if (!sizes_ok(B, T, H, K, V, num_seqs) || !cp_flags_ok(flags)) return 0;
+  const int n_max = kda::cp_max_segments(T, H, V, num_seqs, varlen != 0, flags);
+  return layout_of(B, T, H, K, V, num_seqs, n_max).total;
+}
+
 size_t kda_fwd_workspace_size(int B, int T, int H, int K, int V, int num_seqs) {
-  if (!sizes_ok(B, T, H, K, V, num_seqs)) return 0;
-  return layout_of(B, T, H, K, num_seqs).total;
+  return kda_fwd_workspace_size_ex(B, T, H, K, V, num_seqs, 0, 0u);
 }
 
 const char *kda_status_string(kda_status_t s) {
@@ -300,13 +340,14 @@ kda_status_t kda_fwd_ex(const void *q, const void *k, const void *v, const void 
     return KDA_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (num_seqs == 0) return KDA_OK;
-  const Layout L = layout_of(B, T, H, K, num_seqs);
+  const Layout L = layout_of(B, T, H, K, V, num_seqs,
+                             kda::cp_max_segments(T, H, V, num_seqs, cu_seqlens != nullptr, flags));
   Scratch scr;
   st = get_scratch(workspace, workspace_bytes, L.total, s, scr);
   if (st != KDA_OK) return st;
   kda::Problem p;
   st = fill_problem(p, L, scr.ptr, q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
-                    final_state, cu_seqlens, B, T, H, K, V, num_seqs, flags, o);
+                    final_state, cu_seqlens, B, T, H, K, V, num_seqs, flags & ~kda::kCpFlagsMask, o);
   auto mark = [&](void *ev) {
     if (st == KDA_OK && ev) st = from_cuda(cudaEventRecord(static_cast<cudaEvent_t>(ev), s));
   };
@@ -327,14 +368,36 @@ kda_status_t kda_fwd_ex(const void *q, const void *k, const void *v, const void 
   kda::TmaMaps maps;
   std::memset(&maps, 0, sizeof maps);
   const int bv = kda::recur_slice_width(p);
-  if (st == KDA_OK && T > 0 && !encode_token_map(&maps.v, v, V, H, T, B, bv)) st = KDA_ERR_CUDA;
-  if (st == KDA_OK) {
+  p.n_seg = cp_segments_of(L.n_seg_max, flags, T, H, K, V, num_seqs, bv);
+  const int map_bv = p.n_seg >= 2 ? 64 : bv;
+  if (st == KDA_OK && T > 0 && !encode_token_map(&maps.v, v, V, H, T, B, map_bv)) st = KDA_ERR_CUDA;
+  if (st == KDA_OK && p.n_seg >= 2) {
+    NvtxRange r("kda K2 recurrence, context parallel");
+    st = from_cuda(kda::launch_recur_segments(p, maps, 1, s, !split));
+    if (st == KDA_OK) st = from_cuda(kda::launch_cp_combine(p, s));
+    if (st == KDA_OK) st = from_cuda(kda::launch_recur_segments(p, maps, 2, s, false));
+  } else if (st == KDA_OK) {
     NvtxRange r("kda K2 recurrence");
     st = from_cuda(kda::launch_recur(p, maps, bv, s, !split));
   }
   mark(events ? events->recur_done : nullptr);
   release_scratch(scr, s);
   return st;
+}
+
+kda_status_t kda_fwd_plan(int B, int T, int H, int K, int V, int num_seqs, int varlen, uint32_t flags,
+                          int *n_segments, int *slice_width) {
+  if (!sizes_ok(B, T, H, K, V, num_seqs) || (flags & ~kAllFlags) || !cp_flags_ok(flags))
+    return KDA_ERR_INVALID_ARG;
+  if ((K != 64 && K != 128) || (V != 64 && V != 128)) return KDA_ERR_UNSUPPORTED;
+  const int sms = kda::device_sm_count();
+  if (sms <= 0) return KDA_ERR_CUDA;
+  const int bv = kda::slice_width_for(num_seqs, H, V, sms);
+  const int n_max = kda::cp_max_segments(T, H, V, num_seqs, varlen != 0, flags);
+  const int n_seg = cp_segments_of(n_max, flags, T, H, K, V, num_seqs, bv);
+  if (n_segments) *n_segments = n_seg;
+  if (slice_width) *slice_width = n_seg >= 2 ? 64 : bv;
+  return KDA_OK;
 }
 
 kda_status_t kda_debug_wait_timeout(long long limit_cycles, kda_stream_t stream) {
@@ -364,7 +427,7 @@ kda_status_t kda_debug_chunk_matrices(const void *q, const void *k, const void *
   if (!chunk_mats || !aligned(chunk_mats, 16)) return KDA_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (num_seqs == 0) return KDA_OK;
-  const Layout L = layout_of(B, T, H, K, num_seqs);
+  const Layout L = layout_of(B, T, H, K, K, num_seqs, 0);
   Scratch scr;
   st = get_scratch(workspace, workspace_bytes, L.total, s, scr);
   if (st != KDA_OK) return st;

@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "exp2_poly.cuh"
@@ -27,6 +28,7 @@ constexpr float kNormEps = 1e-6f;   // L2-norm epsilon inside the square root
 constexpr int kDevOk = 0;
 constexpr int kDevBadCuSeqlens = 1;
 constexpr int kDevWaitTimeout = 2;
+constexpr int kDevNonFinite = 3;     // the recurrence's last state of a (sequence, head) is not finite
 
 // Variant flags (mirrors KDA_GATE_PER_HEAD, KDA_BETA_F32, KDA_STATE_BF16, KDA_STATE_KV in
 // include/kda.h).
@@ -35,6 +37,11 @@ constexpr uint32_t kBetaF32 = 0x2u;       // beta logits in fp32
 constexpr uint32_t kStateBf16 = 0x4u;     // initial / final state in bf16
 constexpr uint32_t kStateKV = 0x8u;       // state layout [N,H,K,V] instead of [N,H,V,K]
 constexpr uint32_t kExp2Poly = 0x10u;     // per-token decays 2^la by a polynomial on the FMA pipe
+// Context parallelism (mirrors KDA_CP_OFF and KDA_CP_SEGMENTS(n) in include/kda.h): off, or forced
+// with n segments in bits 8..15; otherwise chosen by the host plan (kda_cp.cu).
+constexpr uint32_t kCpOff = 0x20u;
+constexpr int kCpSegShift = 8;
+constexpr uint32_t kCpFlagsMask = kCpOff | (0xFFu << kCpSegShift);
 
 struct Problem {
   const __nv_bfloat16 *q, *k, *v, *g;  // g [B,T,H,K], or [B,T,H] with kGatePerHead
@@ -60,7 +67,22 @@ struct Problem {
   int nc_fixed;                      // ceil(T / C) in fixed-length mode
   long long max_chunks;
   uint32_t flags;                    // variant flags above
+  // Context parallelism (kda_cp.cu): every sequence is cut into n_seg segments of whole chunks,
+  // segment g holding chunks [n_c g / n_seg, n_c (g + 1) / n_seg) of its n_c.
+  //   seg_state [N][n_seg][H][V + K][K] fp32: end state of each segment run from zero (value
+  //             columns 0..V-1) and its transition (columns V + j: the state reached from the
+  //             unit start column e_j with v = 0); for segment 0, the true end state (V columns)
+  //   seg_start [N][n_seg][H][V][K] fp32: true start state of each segment
+  int n_seg;
+  float *seg_state;
+  float *seg_start;
 };
+
+// Chunk range [lo, hi) of segment g of a sequence of n_c chunks cut into n_seg segments.
+__host__ __device__ inline void segment_chunks(int n_c, int g, int n_seg, int &lo, int &hi) {
+  lo = (int)((long long)n_c * g / n_seg);
+  hi = (int)((long long)n_c * (g + 1) / n_seg);
+}
 
 // TMA descriptor of v, viewed as 4D [B][T][H][V] (innermost V) with a box of
 // (V-slice width) columns x 1 head x 64 tokens x 1 batch row: one copy per chunk and

@@ -59,12 +59,14 @@ extern "C" kda_status_t kda_fwd_noalloc(const void *q, const void *k, const void
                                         int H, int K, int V, int num_seqs, void *o,
                                         kda_stream_t stream) {
   // Size check first, before any CUDA call: reject what the fixed array cannot hold.
-  const size_t need = kda_fwd_workspace_size(B, T, H, K, V, num_seqs);
+  // (context parallelism stays off: its segment states would take scratch from the problem)
+  const size_t need = kda_fwd_workspace_size_ex(B, T, H, K, V, num_seqs, cu_seqlens != nullptr, KDA_CP_OFF);
   if (need > (size_t)KDA_NOALLOC_MAX_SCRATCH) return KDA_ERR_WORKSPACE;
   void *scratch = nullptr;
   const kda_status_t st = scratch_on_current_device(&scratch);
   if (st != KDA_OK) return st;
   // The scratch needs no clearing: every call writes all the scratch it later reads.
-  return kda_fwd(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state, final_state,
-                 cu_seqlens, B, T, H, K, V, num_seqs, o, scratch, (size_t)KDA_NOALLOC_MAX_SCRATCH, stream);
+  return kda_fwd_ex(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state, final_state,
+                    cu_seqlens, B, T, H, K, V, num_seqs, KDA_CP_OFF, o, scratch,
+                    (size_t)KDA_NOALLOC_MAX_SCRATCH, stream, nullptr);
 }

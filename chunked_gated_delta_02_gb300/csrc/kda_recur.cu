@@ -102,7 +102,17 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-template <int K, int BV>
+// MODE selects what one CTA computes (context parallelism, kda_cp.cu, for the two passes):
+//   kPlain      (sequence, head, V slice): the whole sequence from its initial state.
+//   kSegLocal   (sequence, segment g < n_seg - 1, head, slice of [V | K]): segment g from a zero
+//               state (g > 0) or from the initial state (g = 0, value columns only). Columns
+//               V + j carry the transition: start column e_j, v = 0. o is written for g = 0
+//               only; the end state goes to seg_state.
+//   kSegFinal   (sequence, segment g >= 1, head, V slice): segment g from its true start state
+//               (seg_start), writing o, and the final state for the last segment.
+constexpr int kPlain = 0, kSegLocal = 1, kSegFinal = 2;
+
+template <int K, int BV, int MODE>
 __global__ void __launch_bounds__(kRecThreads, 1)
 recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   using Lay = RecLayout<K, BV>;
@@ -118,15 +128,36 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   RecMisc &ms = *reinterpret_cast<RecMisc *>(sm + Lay::misc);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int VT = p.V / BV;
+  // column slices: of V, or of [V | K] in the segment-local pass
+  const int VT = (MODE == kSegLocal ? p.V + K : p.V) / BV;
   const int bid = blockIdx.x;
-  const int r = bid / (p.H * VT);
   const int h = (bid / VT) % p.H;
-  const int v0 = (bid % VT) * BV;
+  const int v0 = (bid % VT) * BV;   // first column of the slice
+  int r = bid / (p.H * VT), seg = 0;
+  if constexpr (MODE != kPlain) {   // r = sequence * (n_seg - 1) + (segment index within the pass)
+    seg = r % (p.n_seg - 1) + (MODE == kSegFinal ? 1 : 0);
+    r /= p.n_seg - 1;
+  }
+  // transition columns (segment-local pass, v0 >= V): v = 0 and the start state is the identity
+  const bool trans = MODE == kSegLocal && v0 >= p.V;
+  if (MODE == kSegLocal && trans && seg == 0) return;   // segment 0 starts from a known state
   pdl_wait();   // the prep kernel (when launched to overlap it) has finished and its writes are visible
   if (p.flag && *p.flag != kDevOk) return;
   const int s = p.cu ? p.order[r] : r;
-  const SeqInfo si = seq_info(p, s);
+  SeqInfo si = seq_info(p, s);
+  if constexpr (MODE != kPlain) {   // the CTA's segment of the sequence
+    int lo, hi;
+    segment_chunks((si.len + kChunk - 1) / kChunk, seg, p.n_seg, lo, hi);
+    si.t0 += lo * kChunk;
+    si.chunk0 += lo;
+    si.len = max(0, min(si.len - lo * kChunk, (hi - lo) * kChunk));
+  }
+  // o is written by the plain kernel, the final pass and segment 0 of the local pass
+  const bool write_o = MODE != kSegLocal || seg == 0;
+  // fp32 [.][cols][K] segment state block of (sequence, segment, head), cols = V + K or V
+  auto seg_block = [&](float *base, int cols) -> float * {
+    return base + (((long long)s * p.n_seg + seg) * p.H + h) * (long long)cols * K;
+  };
   const uint32_t sbase = umma::smem_u32(sm);
   const int nch = (si.len + kChunk - 1) / kChunk;
   const bool is_chain = warp < 4;
@@ -137,6 +168,10 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   for (int b = 0; b < 2; ++b)
     for (int x = tid; x < (int)(2 * Lay::kPanel64 / 16); x += kRecThreads)
       reinterpret_cast<uint4 *>(sm + Lay::kb + b * Lay::kb_size)[x] = make_uint4(0, 0, 0, 0);
+  if (trans)   // v = 0 in transition columns: the fp16 v panels are zeroed once and never converted
+    for (int b = 0; b < 2; ++b)
+      for (int x = tid; x < (int)(Lay::kPanel64 / 16); x += kRecThreads)
+        reinterpret_cast<uint4 *>(sm + Lay::mk + b * Lay::mk_size + Lay::mk_vh)[x] = make_uint4(0, 0, 0, 0);
   if (warp == 0) {
     umma::tmem_alloc(&ms.tmem_slot, kTmemCols);
     umma::tmem_relinquish();
@@ -162,9 +197,18 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   const int stv = (p.flags & kStateKV) ? 1 : K;
   float S[BV];
   if (is_chain && tid < K) {
-    const long long st0 = state_index(p, s, h, tid, v0);
+    if (MODE == kPlain || (MODE == kSegLocal && seg == 0)) {
+      const long long st0 = state_index(p, s, h, tid, v0);
 #pragma unroll
-    for (int v = 0; v < BV; ++v) S[v] = p.init ? state_load(p, st0 + v * stv) : 0.f;
+      for (int v = 0; v < BV; ++v) S[v] = p.init ? state_load(p, st0 + v * stv) : 0.f;
+    } else if (MODE == kSegLocal) {   // zero value columns, identity transition columns
+#pragma unroll
+      for (int v = 0; v < BV; ++v) S[v] = (trans && tid == v0 - p.V + v) ? 1.f : 0.f;
+    } else {   // the segment's true start state from the combine
+      const float *src = seg_block(p.seg_start, p.V) + (long long)v0 * K + tid;
+#pragma unroll
+      for (int v = 0; v < BV; ++v) S[v] = src[(long long)v * K];
+    }
 #pragma unroll
     for (int c = 0; c < BV / 8; ++c) {
       uint4 w;
@@ -187,9 +231,11 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   auto stage_in = [&](int n) {
     const int b = n & 1;
     static_assert(Lay::mk_kg == hand_off_kg(K), "input buffer layout");
-    umma::mbar_arrive_expect_tx(&ms.bar_in[b], (uint32_t)(hand_off_qt(K) + kChunk * BV * 2));
+    umma::mbar_arrive_expect_tx(&ms.bar_in[b], (uint32_t)(hand_off_qt(K) + (trans ? 0 : kChunk * BV * 2)));
     umma::bulk_g2s(sm + Lay::mk + b * Lay::mk_size, slot_of(n), (uint32_t)hand_off_qt(K), &ms.bar_in[b]);
-    umma::tma_load_4d(sm + Lay::rv + b * (kChunk * BV * 2), &maps.v, v0, h, si.t0 + n * kChunk, si.b, &ms.bar_in[b]);
+    if (!trans)
+      umma::tma_load_4d(sm + Lay::rv + b * (kChunk * BV * 2), &maps.v, v0, h, si.t0 + n * kChunk, si.b,
+                        &ms.bar_in[b]);
   };
   auto stage_qt = [&](int n) {
     const int b = n & 1;
@@ -280,7 +326,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
             w.w = pack_half2(-x[8 * hc + 6], -x[8 * hc + 7]);
             *reinterpret_cast<uint4 *>(sm + Lay::Uh + umma::sw128_chunk(tid, (c0 >> 3) + hc)) = w;
           }
-        } else if (tid - kChunk < L && !bad) {
+        } else if (tid - kChunk < L && !bad && write_o) {
           uint4 *dst = reinterpret_cast<uint4 *>(p.o + tok_row(p, si.b, t0 + tid - kChunk, h) * p.V + v0 + c0);
 #pragma unroll
           for (int hc = 0; hc < CW / 8; ++hc) {
@@ -378,7 +424,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       // -- v of chunk n -> fp16, the panel after khat Gamma (vh was last read by D12 of chunk n - 2)
       wait_bar(&ms.bar_in[b], ph);
       in_done += bad ? 0u : 1u;
-      if (L < kChunk) {   // v rows past the sequence end (next packed sequence or zero fill): zero them
+      if (!trans && L < kChunk) {   // v rows past the sequence end (next packed sequence or zero fill): zero them
         for (int x = lt; x < (kChunk - L) * (BV / 8); x += kSubThreads) {
           const int i = L + x / (BV / 8), c8 = x % (BV / 8);
           *reinterpret_cast<uint4 *>(rvb + i * BV + 8 * c8) = make_uint4(0, 0, 0, 0);
@@ -386,7 +432,7 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
         umma::named_bar(sub_bar(sg), kSubThreads);
       }
 #pragma unroll
-      for (int j = 0; j < kChunk * BV / 8 / kSubThreads; ++j) {   // 16-byte chunks of the tile
+      for (int j = 0; j < (trans ? 0 : kChunk * BV / 8 / kSubThreads); ++j) {   // 16-byte chunks of the tile
         const int x = lt + kSubThreads * j;
         const int i = x / (BV / 8), cc = x % (BV / 8);
         const uint4 raw = *reinterpret_cast<const uint4 *>(rvb + i * BV + 8 * cc);
@@ -488,29 +534,44 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
   umma::fence_after_sync();
   if (ms.err) {
     if (tid == 0) atomicExch(p.dev_status, kDevWaitTimeout);
-  } else if (is_chain && p.final_state && tid < K) {
+  } else if (is_chain && tid < K) {
+    // An fp16 overflow of S, U or v (or a non-finite input) leaves inf / NaN in the fp32 state,
+    // which keeps it to the end: one look at the last state reports it (whole warps take part).
+    bool finite = true;
 #pragma unroll
-    for (int v = 0; v < BV; ++v) state_store(p, state_index(p, s, h, tid, v0) + v * stv, S[v]);
+    for (int v = 0; v < BV; ++v) finite &= fabsf(S[v]) <= 3.402823466e38f;
+    if (__any_sync(0xffffffffu, !finite) && lane == 0) atomicExch(p.dev_status, kDevNonFinite);
+    if (MODE == kSegLocal) {   // end state of the segment (or its transition) for the combine
+      float *dst = seg_block(p.seg_state, p.V + K) + (long long)v0 * K + tid;
+#pragma unroll
+      for (int v = 0; v < BV; ++v) dst[(long long)v * K] = S[v];
+    } else if (p.final_state && (MODE == kPlain || seg == p.n_seg - 1)) {
+#pragma unroll
+      for (int v = 0; v < BV; ++v) state_store(p, state_index(p, s, h, tid, v0) + v * stv, S[v]);
+    }
   }
   if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int K, int BV>
+template <int K, int BV, int MODE>
 static cudaError_t launch_recur_t(const Problem &p, const TmaMaps &maps, cudaStream_t stream, bool overlap) {
   const size_t smem = RecLayout<K, BV>::bytes;
   static_assert(sizeof(RecMisc) <= 1024, "misc block");
   static PerDeviceOnce attr;
   cudaError_t e = attr([&](int) {
-    return cudaFuncSetAttribute(recur_tc_kernel<K, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    return cudaFuncSetAttribute(recur_tc_kernel<K, BV, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem);
   });
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)p.N * p.H * (p.V / BV);
-  return launch_kernel(recur_tc_kernel<K, BV>, dim3((unsigned)grid), dim3(kRecThreads), smem, stream, overlap, p,
-                       maps);
+  const int cols = MODE == kSegLocal ? p.V + K : p.V;
+  const long long jobs = MODE == kPlain ? (long long)p.N : (long long)p.N * (p.n_seg - 1);
+  const long long grid = jobs * p.H * (cols / BV);
+  return launch_kernel(recur_tc_kernel<K, BV, MODE>, dim3((unsigned)grid), dim3(kRecThreads), smem, stream,
+                       overlap, p, maps);
 }
 
-// V-slice width: 64 unless that leaves fewer than about 80% of the SMs with a CTA.
-int recur_slice_width(const Problem &p) {
+// SM count of the current device (looked up once per device), or 0 if it cannot be read.
+int device_sm_count() {
   static PerDeviceOnce once;
   static std::atomic<int> sm_count[64];
   int sms = 0;
@@ -523,27 +584,47 @@ int recur_slice_width(const Problem &p) {
   });
   if (e != cudaSuccess) {
     cudaGetLastError();
-    return kBVWide;
+    return 0;
   }
   if (sms == 0) {   // looked up by an earlier call on this device
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) sms = sm_count[dev].load(std::memory_order_relaxed);
     if (sms == 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
       cudaGetLastError();
-      return kBVWide;
+      return 0;
     }
   }
-  const long long wide_ctas = (long long)p.N * p.H * (p.V / kBVWide);
+  return sms;
+}
+
+// V-slice width: 64 unless that leaves fewer than about 80% of the SMs with a CTA.
+int slice_width_for(long long N, int H, int V, int sms) {
+  if (sms <= 0) return kBVWide;
+  const long long wide_ctas = N * H * (V / kBVWide);
   return (5 * wide_ctas >= 4LL * sms) ? kBVWide : kBVNarrow;
 }
+int recur_slice_width(const Problem &p) { return slice_width_for(p.N, p.H, p.V, device_sm_count()); }
 
 cudaError_t launch_recur(const Problem &p, const TmaMaps &maps, int bv, cudaStream_t stream, bool overlap) {
   if (p.N == 0) return cudaSuccess;
   if (bv == kBVNarrow)
-    return p.K == 64 ? launch_recur_t<64, kBVNarrow>(p, maps, stream, overlap)
-                     : launch_recur_t<128, kBVNarrow>(p, maps, stream, overlap);
-  return p.K == 64 ? launch_recur_t<64, kBVWide>(p, maps, stream, overlap)
-                   : launch_recur_t<128, kBVWide>(p, maps, stream, overlap);
+    return p.K == 64 ? launch_recur_t<64, kBVNarrow, kPlain>(p, maps, stream, overlap)
+                     : launch_recur_t<128, kBVNarrow, kPlain>(p, maps, stream, overlap);
+  return p.K == 64 ? launch_recur_t<64, kBVWide, kPlain>(p, maps, stream, overlap)
+                   : launch_recur_t<128, kBVWide, kPlain>(p, maps, stream, overlap);
+}
+
+// The two recurrence passes of context parallelism (64-column slices): pass 1 runs every segment
+// but the last from a zero (or, for segment 0, the initial) state with the transition columns;
+// pass 2 runs every segment but the first from the start state the combine formed.
+cudaError_t launch_recur_segments(const Problem &p, const TmaMaps &maps, int pass, cudaStream_t stream,
+                                  bool overlap) {
+  if (p.N == 0 || p.n_seg < 2) return cudaSuccess;
+  if (pass == 1)
+    return p.K == 64 ? launch_recur_t<64, kBVWide, kSegLocal>(p, maps, stream, overlap)
+                     : launch_recur_t<128, kBVWide, kSegLocal>(p, maps, stream, overlap);
+  return p.K == 64 ? launch_recur_t<64, kBVWide, kSegFinal>(p, maps, stream, overlap)
+                   : launch_recur_t<128, kBVWide, kSegFinal>(p, maps, stream, overlap);
 }
 
 }  // namespace kda

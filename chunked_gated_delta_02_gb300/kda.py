@@ -18,13 +18,32 @@ import torch
 from ._lib import check, lib
 
 __all__ = ["fwd", "fwd_noalloc", "workspace_size", "debug_chunk_matrices", "device_status", "max_chunks",
-           "NOALLOC_MAX_SCRATCH", "GATE_PER_HEAD", "BETA_F32", "STATE_BF16", "STATE_KV", "EXP2_POLY"]
+           "NOALLOC_MAX_SCRATCH", "GATE_PER_HEAD", "BETA_F32", "STATE_BF16", "STATE_KV", "EXP2_POLY",
+           "CP_OFF", "CP_SEGMENTS", "plan"]
 
 # Size of the library's fixed scratch array used by fwd_noalloc (KDA_NOALLOC_MAX_SCRATCH).
 NOALLOC_MAX_SCRATCH = 16 * 1024 * 1024
 
 # Variant flags of kda_fwd_ex (include/kda.h).
 GATE_PER_HEAD, BETA_F32, STATE_BF16, STATE_KV, EXP2_POLY = 0x1, 0x2, 0x4, 0x8, 0x10
+# Context parallelism (include/kda.h): off, or forced with n segments per sequence.
+CP_OFF = 0x20
+
+
+def CP_SEGMENTS(n: int) -> int:
+    return (int(n) & 0xFF) << 8
+
+
+def _cp_flags(context_parallel) -> int:
+    """None: chosen by the library; False: off; an int n >= 2: n segments per sequence."""
+    if context_parallel is None or context_parallel is True:
+        return 0
+    if context_parallel is False:
+        return CP_OFF
+    n = int(context_parallel)
+    if not 2 <= n <= 64:
+        raise ValueError("context_parallel must be None, False, True or a segment count in [2, 64]")
+    return CP_SEGMENTS(n)
 
 
 class _StageEvents(ctypes.Structure):
@@ -41,11 +60,14 @@ def _stream_ptr(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _need(t, name, dtype, shape=None):
+def _need(t, name, dtype, shape=None, device=None):
+    """Type, dtype, contiguity, shape and device of one tensor argument. The device is compared
+    with the reference device (q's) here; that q itself is on a GPU is checked last, so that
+    every argument is refused for its own fault."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device} (the device of q), got {t.device}")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -54,8 +76,66 @@ def _need(t, name, dtype, shape=None):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
-def workspace_size(B: int, T: int, H: int, K: int, V: int, num_seqs: int) -> int:
-    return int(lib().kda_fwd_workspace_size(B, T, H, K, V, num_seqs))
+def _on_gpu(q):
+    if q.device.type != "cuda":
+        raise ValueError("q must be a CUDA tensor (there is no CPU path)")
+
+
+def _check_inputs(q, k, v, g, beta, A_log, dt_bias, cu_seqlens):
+    """Checks the token tensors and the gate parameters of a forward call. Returns
+    (B, T, H, K, V, N, flags) with the variant flags the arguments select."""
+    if not isinstance(q, torch.Tensor) or q.dim() != 4:
+        raise ValueError("q must be a 4-D torch.Tensor [B,T,H,K]")
+    if not isinstance(v, torch.Tensor) or v.dim() != 4:
+        raise ValueError("v must be a 4-D torch.Tensor [B,T,H,V]")
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dev = q.device
+    flags = 0
+    _need(q, "q", torch.bfloat16, None, dev)
+    _need(k, "k", torch.bfloat16, (B, T, H, K), dev)
+    if isinstance(g, torch.Tensor) and g.dim() == 3:
+        flags |= GATE_PER_HEAD
+        _need(g, "g", torch.bfloat16, (B, T, H), dev)
+    else:
+        _need(g, "g", torch.bfloat16, (B, T, H, K), dev)
+    _need(v, "v", torch.bfloat16, (B, T, H, V), dev)
+    if isinstance(beta, torch.Tensor) and beta.dtype == torch.float32:
+        flags |= BETA_F32
+        _need(beta, "beta", torch.float32, (B, T, H), dev)
+    else:
+        _need(beta, "beta", torch.bfloat16, (B, T, H), dev)
+    _need(A_log, "A_log", torch.float32, (H,), dev)
+    if dt_bias is not None:
+        _need(dt_bias, "dt_bias", torch.float32, None, dev)
+        want = H if flags & GATE_PER_HEAD else H * K
+        if dt_bias.numel() != want:
+            raise ValueError(f"dt_bias must hold {want} values")
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, None, dev)
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+            raise ValueError("cu_seqlens must be a 1-D tensor of N + 1 offsets")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    return B, T, H, K, V, N, flags
+
+
+def workspace_size(B: int, T: int, H: int, K: int, V: int, num_seqs: int, varlen: bool = False,
+                   flags: int = 0) -> int:
+    """Scratch bytes of a forward call (kda_fwd_workspace_size_ex): `flags` as passed to the call
+    (only the context-parallel flags matter), `varlen` whether it passes cu_seqlens."""
+    return int(lib().kda_fwd_workspace_size_ex(B, T, H, K, V, num_seqs, int(bool(varlen)), flags))
+
+
+def plan(B: int, T: int, H: int, K: int, V: int, num_seqs: int, varlen: bool = False, context_parallel=None):
+    """(segments per sequence, V columns per recurrence CTA) that a forward call with these sizes
+    would use on the current device; 0 segments is the plain recurrence (kda_fwd_plan)."""
+    n, bv = ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib().kda_fwd_plan(B, T, H, K, V, num_seqs, int(bool(varlen)), _cp_flags(context_parallel),
+                            ctypes.byref(n), ctypes.byref(bv))
+    check("kda_fwd_plan", rc)
+    return int(n.value), int(bv.value)
 
 
 def max_chunks(B: int, T: int, num_seqs: int) -> int:
@@ -70,7 +150,7 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
         final_state: Optional[torch.Tensor] = None,
         events=None, state_layout: str = "vk",
         state_dtype: Optional[torch.dtype] = None,
-        exp2_poly: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+        exp2_poly: bool = False, context_parallel=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """KDA chunked forward on the GPU.
 
     q, k: bf16 [B,T,H,K]; v: bf16 [B,T,H,V]; g: bf16 [B,T,H,K], or [B,T,H] for one
@@ -82,6 +162,9 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
     initial_state (default fp32; with an initial_state, its dtype).
     exp2_poly: evaluate the per-token decays with the FMA-pipe polynomial
     instead of the SFU exponential (an implementation option, KDA_EXP2_POLY).
+    context_parallel: None (the library decides), False (off) or a segment count
+    n in [2, 64] (forced): intracard context parallelism of long fixed-length
+    sequences (KDA_CP_OFF / KDA_CP_SEGMENTS(n)); ignored with cu_seqlens.
     Returns (o bf16 [B,T,H,V], final_state in the state layout and dtype, or None).
     events: optional (prep_start, prep_done, recur_done) torch.cuda.Event triple
     recorded on the current stream at the kernel boundaries (profiling only; a None
@@ -89,31 +172,10 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
     overlaps the end of the prep kernel, as without events; with it the two run
     one after the other, so that the event splits their times.
     """
-    B, T, H, K = q.shape
-    V = v.shape[-1]
-    flags = EXP2_POLY if exp2_poly else 0
-    _need(q, "q", torch.bfloat16)
-    _need(k, "k", torch.bfloat16, (B, T, H, K))
-    if g.dim() == 3:
-        flags |= GATE_PER_HEAD
-        _need(g, "g", torch.bfloat16, (B, T, H))
-    else:
-        _need(g, "g", torch.bfloat16, (B, T, H, K))
-    _need(v, "v", torch.bfloat16, (B, T, H, V))
-    if beta.dtype == torch.float32:
-        flags |= BETA_F32
-    _need(beta, "beta", beta.dtype if beta.dtype == torch.float32 else torch.bfloat16, (B, T, H))
-    _need(A_log, "A_log", torch.float32, (H,))
-    if dt_bias is not None:
-        _need(dt_bias, "dt_bias", torch.float32)
-        want = H if flags & GATE_PER_HEAD else H * K
-        if dt_bias.numel() != want:
-            raise ValueError(f"dt_bias must hold {want} values")
-    if cu_seqlens is not None:
-        _need(cu_seqlens, "cu_seqlens", torch.int32)
-        N = cu_seqlens.numel() - 1
-    else:
-        N = B
+    B, T, H, K, V, N, flags = _check_inputs(q, k, v, g, beta, A_log, dt_bias, cu_seqlens)
+    if exp2_poly:
+        flags |= EXP2_POLY
+    flags |= _cp_flags(context_parallel)
     if state_layout not in ("vk", "kv"):
         raise ValueError("state_layout must be 'vk' ([N,H,V,K]) or 'kv' ([N,H,K,V])")
     sshape = (N, H, V, K) if state_layout == "vk" else (N, H, K, V)
@@ -124,18 +186,23 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
         raise TypeError("the state must be float32 or bfloat16")
     if sdt == torch.bfloat16:
         flags |= STATE_BF16
+    dev = q.device
     if initial_state is not None:
-        _need(initial_state, "initial_state", sdt, sshape)
+        _need(initial_state, "initial_state", sdt, sshape, dev)
     if scale is None:
         scale = K ** -0.5
-    dev = q.device
+    if out is not None:
+        _need(out, "out", torch.bfloat16, (B, T, H, V), dev)
+    if output_final_state and final_state is not None:
+        _need(final_state, "final_state", sdt, sshape, dev)
+    if workspace is not None:
+        _need(workspace, "workspace", workspace.dtype, None, dev)
+    _on_gpu(q)
     o = out if out is not None else torch.empty(B, T, H, V, dtype=torch.bfloat16, device=dev)
-    _need(o, "out", torch.bfloat16, (B, T, H, V))
     fs = None
     if output_final_state:
         fs = final_state if final_state is not None else torch.empty(*sshape, dtype=sdt, device=dev)
-        _need(fs, "final_state", sdt, sshape)
-    need = workspace_size(B, T, H, K, V, N)
+    need = workspace_size(B, T, H, K, V, N, cu_seqlens is not None, flags)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     elif workspace.numel() * workspace.element_size() < need:
@@ -166,12 +233,22 @@ def fwd_noalloc(q, k, v, g, beta, A_log, dt_bias=None, lower_bound=-5.0, scale=N
     Calls that overlap on the GPU share the array and race: keep them ordered.
     Returns (out, final_state).
     """
-    B, T, H, K = q.shape
-    V = v.shape[-1]
-    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
-    for t, name in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (A_log, "A_log"), (out, "out")):
-        if t is None or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    B, T, H, K, V, N, flags = _check_inputs(q, k, v, g, beta, A_log, dt_bias, cu_seqlens)
+    if flags:
+        raise TypeError("fwd_noalloc takes the default variant only: g [B,T,H,K] and bf16 beta")
+    dev = q.device
+    sshape = (N, H, V, K)
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, sshape, dev)
+    if final_state is not None:
+        _need(final_state, "final_state", torch.float32, sshape, dev)
+    if out is None:
+        raise ValueError("fwd_noalloc needs the caller's output buffer `out`")
+    _need(out, "out", torch.bfloat16, (B, T, H, V), dev)
+    _on_gpu(q)
+    need = workspace_size(B, T, H, K, V, N, cu_seqlens is not None, CP_OFF)
+    if need > NOALLOC_MAX_SCRATCH:
+        raise ValueError(f"problem needs {need} bytes of scratch, more than the fixed {NOALLOC_MAX_SCRATCH}")
     if scale is None:
         scale = K ** -0.5
     with torch.cuda.device(q.device):

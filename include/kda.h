@@ -69,6 +69,17 @@ typedef enum {
 #define KDA_DEVICE_OK 0
 #define KDA_DEVICE_BAD_CU_SEQLENS 1   /* cu_seqlens[0] != 0, decreasing, or cu_seqlens[N] != T */
 #define KDA_DEVICE_WAIT_TIMEOUT 2     /* a bounded pipeline wait in a kernel gave up */
+/*
+ * The recurrence ended with a non-finite state for some (sequence, head): an
+ * input was not finite, or a value went past the fp16 range (|x| > 65504) of
+ * the recurrence's tensor-core operands. Those operands are the state S, the
+ * residuals U = v - prediction and v itself, rounded to fp16 once per chunk;
+ * an overflow there turns into inf / NaN, which the fp32 state keeps, so a
+ * check of every (sequence, head)'s last state catches it. The check runs
+ * whether or not final_state is requested. o of that (sequence, head) is then
+ * not valid.
+ */
+#define KDA_DEVICE_NONFINITE 3
 
 /* Tokens per chunk of the chunked algorithm. */
 #define KDA_CHUNK 64
@@ -85,6 +96,17 @@ typedef enum {
  * about 64.5 KiB per chunk of 64 tokens and head at K = 128.
  */
 KDA_API size_t kda_fwd_workspace_size(int B, int T, int H, int K, int V, int num_seqs);
+
+/*
+ * kda_fwd_workspace_size() for a call of kda_fwd_ex() with these flags: the
+ * context-parallel flags (KDA_CP_OFF, KDA_CP_SEGMENTS(n)) change the scratch
+ * the call needs; the other flags do not. varlen is nonzero when the call will
+ * pass cu_seqlens (context parallelism then never applies). Returns 0 when the
+ * sizes or flags are invalid. kda_fwd_workspace_size(...) is
+ * kda_fwd_workspace_size_ex(..., 0, 0): enough for kda_fwd() in either mode.
+ */
+KDA_API size_t kda_fwd_workspace_size_ex(int B, int T, int H, int K, int V, int num_seqs, int varlen,
+                                         uint32_t flags);
 
 /*
  * KDA chunked forward.
@@ -155,6 +177,31 @@ KDA_API kda_status_t kda_fwd(const void *q, const void *k, const void *v, const 
 #define KDA_STATE_BF16 0x4u
 #define KDA_STATE_KV 0x8u
 #define KDA_EXP2_POLY 0x10u
+
+/*
+ * Intracard context parallelism (the FlashKDA intracard CP of the cuLA README
+ * mirror, section "Benchmarks"; the gate-driven intracard context parallelism
+ * of the FlashQLA page, section "핵심 기능"), an implementation option that does
+ * not change the operation. Each sequence is cut into segments of whole
+ * chunks that run in parallel: a first pass runs every segment from a zero
+ * state and also forms its K x K state transition, a small combine pass chains
+ * the segments' start states, and a second pass reruns every segment from its
+ * true start state. It costs up to about three times the recurrence work and
+ * pays only when the plain recurrence leaves most SMs idle (few long
+ * sequences and heads). Fixed-length batches only: with cu_seqlens it is never
+ * used.
+ *
+ *   (default)            chosen per call from the sizes and the SM count, where
+ *                        the library's estimate shows a clear gain.
+ *   KDA_CP_OFF           never.
+ *   KDA_CP_SEGMENTS(n)   always, with n segments per sequence, n in [2, 64]
+ *                        (segments past the end of a short sequence are empty).
+ * The workspace must then be sized by kda_fwd_workspace_size_ex() with the
+ * same flags: segment states need (2 V + K) K fp32 values per (sequence,
+ * segment, head).
+ */
+#define KDA_CP_OFF 0x20u
+#define KDA_CP_SEGMENTS(n) ((((uint32_t)(n)) & 0xFFu) << 8)
 
 /*
  * Stage timing hooks for kda_fwd_with_events(): CUDA events (cudaEvent_t,
@@ -244,7 +291,9 @@ KDA_API kda_status_t kda_debug_chunk_matrices(const void *q, const void *k, cons
  * workspace pair; the caller still passes every input and output buffer.
  *
  * Limit: the problem must fit in KDA_NOALLOC_MAX_SCRATCH bytes of scratch,
- * i.e. kda_fwd_workspace_size(B, T, H, K, V, num_seqs) <= KDA_NOALLOC_MAX_SCRATCH
+ * i.e. kda_fwd_workspace_size_ex(B, T, H, K, V, num_seqs, cu_seqlens != NULL,
+ * KDA_CP_OFF) <= KDA_NOALLOC_MAX_SCRATCH: this entry point never uses context
+ * parallelism, whose segment states would take scratch away from the problem
  * (about 8 MiB per head per 8192 tokens at K = V = 128: B=1, T=8192 fits H = 1,
  * B=1, T=2048 fits H <= 7).
  * Larger problems are rejected with KDA_ERR_WORKSPACE before anything runs.
@@ -266,6 +315,18 @@ KDA_API kda_status_t kda_fwd_noalloc(const void *q, const void *k, const void *v
                                      float lower_bound, float scale, const float *initial_state,
                                      float *final_state, const int32_t *cu_seqlens, int B, int T,
                                      int H, int K, int V, int num_seqs, void *o, kda_stream_t stream);
+
+/*
+ * The launch plan kda_fwd_ex() would use on the current device for these sizes
+ * and flags: *n_segments gets the number of context-parallel segments per
+ * sequence (0 for the plain recurrence) and *slice_width the V columns per
+ * recurrence CTA (64 or 16). Either pointer may be NULL. varlen is nonzero for
+ * a call with cu_seqlens. (A query with no counterpart on the pages; it reads
+ * the device's SM count.) Returns KDA_OK, KDA_ERR_INVALID_ARG,
+ * KDA_ERR_UNSUPPORTED or KDA_ERR_CUDA (no device).
+ */
+KDA_API kda_status_t kda_fwd_plan(int B, int T, int H, int K, int V, int num_seqs, int varlen, uint32_t flags,
+                                  int *n_segments, int *slice_width);
 
 /* Upper bound on the number of 64-token chunks over all sequences. */
 KDA_API int64_t kda_max_chunks(int B, int T, int num_seqs);

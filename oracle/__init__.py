@@ -17,5 +17,5 @@ Every function is pinned by tests under tests/ (test_oracle_pins.py) against
 closed forms, invariants, special cases that reduce to library routines,
 hand-derived golden values and brute force on tiny inputs.
 """
-from .kda_ref import kda_fwd_ref, sigmoid, gate_log_decay, l2_normalize, to_f64, bf16_round  # noqa: F401
+from .kda_ref import kda_fwd_ref, sigmoid, gate_log_decay, l2_normalize, to_f64  # noqa: F401
 from .chunked_ref import kda_fwd_chunked, chunk_quantities, forward_substitution_inverse  # noqa: F401

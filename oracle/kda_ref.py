@@ -41,8 +41,7 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["sigmoid", "gate_log_decay", "l2_normalize", "kda_fwd_ref",
-           "to_f64", "bf16_round"]
+__all__ = ["sigmoid", "gate_log_decay", "l2_normalize", "kda_fwd_ref", "to_f64"]
 
 
 def to_f64(x) -> np.ndarray:
@@ -54,13 +53,6 @@ def to_f64(x) -> np.ndarray:
     except ImportError:  # pragma: no cover
         pass
     return np.asarray(x, dtype=np.float64)
-
-
-def bf16_round(x: np.ndarray) -> np.ndarray:
-    """Round float64 values to the nearest bfloat16 (ties to even), as float64."""
-    import torch
-    return torch.from_numpy(np.asarray(x, dtype=np.float64)).to(torch.bfloat16).to(
-        torch.float64).numpy()
 
 
 def sigmoid(x):

@@ -66,24 +66,50 @@ def check_full(inp: dict, what=""):
     return assert_parity(o, fs, ref_o, ref_f, what)
 
 
-def gather_pairs(inp, o_gpu, fs_gpu, pairs):
-    """GPU outputs of the chosen (sequence, head) pairs, in the oracle's compact order."""
-    cu = inp["cu_seqlens"]
-    o = o_gpu.float().cpu()
-    outs = []
-    for s, h in pairs:
-        if cu is None:
-            outs.append(o[s, :, h].double().numpy())
-        else:
-            outs.append(o[0, int(cu[s]):int(cu[s + 1]), h].double().numpy())
-    fin = fs_gpu.cpu()[[s for s, _ in pairs], [h for _, h in pairs]].double().numpy()
-    return np.concatenate(outs, 0), fin
+def check_all_pairs(inp, o_gpu, fs_gpu, what="", max_token_heads=1 << 20):
+    """Every (sequence, head) of a large workload against the C oracle, element by element.
 
-
-def check_pairs(inp, o_gpu, fs_gpu, pairs, what=""):
+    The oracle runs on batches of (sequence, head) pairs (at most max_token_heads token-heads, at
+    least one pair per host thread) so that host memory stays bounded; the squared errors and
+    norms are summed over the batches, so the rel-L2 figures are those of the whole tensors and
+    max-abs is the largest error of any element of o."""
     from oracle import c_oracle
-    ref_o, ref_f = c_oracle.kda_fwd_c(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["A_log"],
-                                      inp["dt_bias"], inp["lower_bound"], inp["scale"],
-                                      inp["initial_state"], inp["cu_seqlens"], pairs=pairs)
-    go, gf = gather_pairs(inp, o_gpu, fs_gpu, pairs)
-    return assert_parity(go, gf, np.concatenate(ref_o, 0), ref_f, what)
+    cu = inp["cu_seqlens"]
+    N, H = inp["N"], inp["H"]
+    lens = [int(cu[i + 1] - cu[i]) for i in range(N)] if cu is not None else [inp["T"]] * N
+    threads = c_oracle.default_threads()
+    o = o_gpu.float().cpu()
+    fs = fs_gpu.cpu().double().numpy()
+    pairs = [(s, h) for s in range(N) for h in range(H)]
+    num_o = den_o = num_s = den_s = 0.0
+    max_abs = 0.0
+    i = 0
+    while i < len(pairs):
+        batch, th = [], 0
+        while i < len(pairs) and (len(batch) < threads or th + lens[pairs[i][0]] <= max_token_heads):
+            batch.append(pairs[i])
+            th += lens[pairs[i][0]]
+            i += 1
+        ref_o, ref_f = c_oracle.kda_fwd_c(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["A_log"],
+                                          inp["dt_bias"], inp["lower_bound"], inp["scale"],
+                                          inp["initial_state"], cu, pairs=batch, n_threads=threads)
+        for j, (s, h) in enumerate(batch):
+            g = (o[s, :, h] if cu is None else o[0, int(cu[s]):int(cu[s + 1]), h]).double().numpy()
+            r = ref_o[j]
+            assert np.all(np.isfinite(g)), f"{what}: non-finite o in (sequence {s}, head {h})"
+            d = g - r
+            num_o += float(np.sum(d * d))
+            den_o += float(np.sum(r * r))
+            if d.size:
+                max_abs = max(max_abs, float(np.max(np.abs(d))))
+            gf = fs[s, h]
+            assert np.all(np.isfinite(gf)), f"{what}: non-finite final_state in (sequence {s}, head {h})"
+            df = gf - ref_f[j]
+            num_s += float(np.sum(df * df))
+            den_s += float(np.sum(ref_f[j] * ref_f[j]))
+    eo = (num_o / den_o) ** 0.5 if den_o > 0 else num_o ** 0.5
+    es = (num_s / den_s) ** 0.5 if den_s > 0 else num_s ** 0.5
+    assert eo <= TOL_O_REL and max_abs <= TOL_O_MAXABS, \
+        f"{what}: o rel-L2 {eo:.3e} (<= {TOL_O_REL}), max-abs {max_abs:.3e} (<= {TOL_O_MAXABS})"
+    assert es <= TOL_S_REL, f"{what}: final_state rel-L2 {es:.3e} (<= {TOL_S_REL})"
+    return eo, max_abs, es

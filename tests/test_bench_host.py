@@ -97,3 +97,19 @@ def test_reference_arm_json_line(monkeypatch):
     assert line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_each_kernel_is_credited_with_its_own_bytes():
+    """The prep kernel is credited with q, k, g and beta (770 B per token-head at K = 128), the
+    recurrence kernel with v, o and the state; together they are the path's algorithmic bytes."""
+    inp = dict(B=2, T=2048, H=32, K=128, V=128, N=2, initial_state=None)
+    th = 2 * 2048 * 32
+    ab = bench.kernel_algorithmic_bytes(inp)
+    assert ab["prep"] == th * 770
+    assert ab["recurrence"] == th * 512 + 2 * 32 * 128 * 128 * 4
+    assert ab["prep"] + ab["recurrence"] == bench.algorithmic_bytes(inp) == th * 1282 + 2 * 32 * 128 * 128 * 4
+    roofs = bench.kernel_rooflines(inp, 0.0907, 0.0581, 6680.8, "test", "no-such-workload")
+    assert roofs[0]["kernel"].startswith("prep")
+    assert abs(roofs[0]["frac"] - th * 770 / 90.7e-6 / 1e9 / 6680.8) < 1e-9
+    assert abs(roofs[0]["frac"] - 0.1666) < 1e-3
+    assert roofs[0]["traffic"] is None and roofs[0]["traffic_over_algorithmic"] is None

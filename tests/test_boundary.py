@@ -120,8 +120,37 @@ def _call_ex(lib, flags, **kw):
 
 
 def test_fwd_ex_rejects_unknown_flags_without_launch(lib):
-    for flags in (0x20, 0x80000000, 0x3F):
+    for flags in (0x40, 0x80, 0x10000, 0x80000000, 0x7F):
         assert _call_ex(lib, flags) == 1
+    # context parallelism: KDA_CP_SEGMENTS(n) needs n in [2, 64] and excludes KDA_CP_OFF
+    for flags in (1 << 8, 65 << 8, 255 << 8, 0x20 | (4 << 8)):
+        assert _call_ex(lib, flags) == 1
+
+
+def test_workspace_size_with_context_parallel_flags(lib):
+    CP_OFF = 0x20
+    B, T, H, K, V = 1, 4096, 2, 128, 128
+    plain = lib.kda_fwd_workspace_size_ex(B, T, H, K, V, 1, 0, CP_OFF)
+    per_seg = H * (2 * V + K) * K * 4          # segment end state + transition, and start state
+    for n in (2, 3, 7):
+        forced = lib.kda_fwd_workspace_size_ex(B, T, H, K, V, 1, 0, n << 8)
+        assert plain + n * per_seg <= forced <= plain + n * per_seg + 512
+    # never with cu_seqlens: the forced flag changes nothing there
+    assert lib.kda_fwd_workspace_size_ex(B, T, H, K, V, 1, 1, 4 << 8) == plain
+    # the default size covers the automatic choice: few heads of a long sequence reserve segments
+    assert lib.kda_fwd_workspace_size(B, T, H, K, V, 1) >= plain + 2 * per_seg
+    # many heads never use it, and short sequences do not either
+    assert lib.kda_fwd_workspace_size(2, 2048, 32, K, V, 2) == lib.kda_fwd_workspace_size_ex(2, 2048, 32, K, V, 2, 0, CP_OFF)
+    assert lib.kda_fwd_workspace_size(1, 1000, 1, K, V, 1) == lib.kda_fwd_workspace_size_ex(1, 1000, 1, K, V, 1, 0, CP_OFF)
+    assert lib.kda_fwd_workspace_size_ex(B, T, H, K, V, 1, 0, 1 << 8) == 0     # one segment: invalid
+
+
+def test_plan_needs_a_device_and_valid_arguments(lib):
+    import ctypes
+    n, bv = ctypes.c_int(-1), ctypes.c_int(-1)
+    assert lib.kda_fwd_plan(1, 64, 1, 96, 64, 1, 0, 0, ctypes.byref(n), ctypes.byref(bv)) == 2
+    assert lib.kda_fwd_plan(1, 64, 1, 64, 64, 1, 0, 1 << 8, ctypes.byref(n), ctypes.byref(bv)) == 1
+    assert lib.kda_fwd_plan(0, 64, 1, 64, 64, 1, 0, 0, ctypes.byref(n), ctypes.byref(bv)) == 1
 
 
 def test_fwd_ex_variant_alignment_rules(lib):
@@ -135,7 +164,7 @@ def test_fwd_ex_variant_alignment_rules(lib):
     assert _call_ex(lib, BETA_F32, beta=FAKE + 2) == 1
     assert _call_ex(lib, 0, beta=FAKE + 1) == 1
     # the other checks still apply under every flag
-    for flags in (0x1, 0x2, 0x4, 0x8, 0x10, 0x1F):
+    for flags in (0x1, 0x2, 0x4, 0x8, 0x10, 0x1F, 0x20, 4 << 8):
         assert _call_ex(lib, flags, K=96) == 2          # unsupported head dim
         assert _call_ex(lib, flags, lb=-6.0) == 1       # lower bound out of range
         assert _call_ex(lib, flags, init=FAKE + 8) == 1  # state alignment
@@ -152,3 +181,67 @@ def test_python_binding_has_no_cpu_path(lib):
         kda.fwd(q, q, q, q, torch.zeros(B, T, H, dtype=torch.bfloat16), torch.zeros(H), None, -5.0)
     with pytest.raises(ValueError, match="CUDA tensor"):
         kda.fwd_noalloc(q, q, q, q, torch.zeros(B, T, H, dtype=torch.bfloat16), torch.zeros(H), out=q)
+
+
+def _meta_args(B=1, T=64, H=2, K=64, V=64):
+    """Well-formed arguments on the meta device (no storage): the binding's shape, dtype and
+    device checks can run on them without a GPU."""
+    import torch
+    m = dict(device="meta")
+    return dict(q=torch.empty(B, T, H, K, dtype=torch.bfloat16, **m),
+                k=torch.empty(B, T, H, K, dtype=torch.bfloat16, **m),
+                v=torch.empty(B, T, H, V, dtype=torch.bfloat16, **m),
+                g=torch.empty(B, T, H, K, dtype=torch.bfloat16, **m),
+                beta=torch.empty(B, T, H, dtype=torch.bfloat16, **m),
+                A_log=torch.empty(H, dtype=torch.float32, **m),
+                out=torch.empty(B, T, H, V, dtype=torch.bfloat16, **m))
+
+
+@pytest.mark.parametrize("entry", ["fwd", "fwd_noalloc"])
+def test_binding_refuses_each_bad_argument(entry):
+    """Every tensor argument of fwd and fwd_noalloc, optional ones included, is checked for device,
+    dtype, shape and contiguity before the library is called: a host final_state or a wrong-shape
+    out never reaches a kernel."""
+    import torch
+    import chunked_gated_delta_02_gb300 as kda
+    B, T, H, K, V = 1, 64, 2, 64, 64
+    fn = getattr(kda, entry)
+
+    def call(**over):
+        a = _meta_args(B, T, H, K, V)
+        a.update(over)
+        extra = {}
+        for name in ("dt_bias", "initial_state", "final_state", "cu_seqlens"):
+            if name in a:
+                extra[name] = a.pop(name)
+        if entry == "fwd":
+            out = a.pop("out")
+            fs = extra.pop("final_state", None)
+            return fn(a["q"], a["k"], a["v"], a["g"], a["beta"], a["A_log"], out=out, final_state=fs,
+                      output_final_state=fs is not None, **extra)
+        return fn(a["q"], a["k"], a["v"], a["g"], a["beta"], a["A_log"], out=a["out"], **extra)
+
+    meta = torch.device("meta")
+    with pytest.raises(ValueError, match="final_state must be on"):
+        call(final_state=torch.empty(B, H, V, K))                                   # host memory
+    with pytest.raises(ValueError, match="out must have shape"):
+        call(out=torch.empty(B, T, H, V + 1, dtype=torch.bfloat16, device=meta))
+    with pytest.raises(ValueError, match="out must be on"):
+        call(out=torch.empty(B, T, H, V, dtype=torch.bfloat16))
+    with pytest.raises(TypeError, match="final_state must be"):
+        call(final_state=torch.empty(B, H, V, K, dtype=torch.float16, device=meta))
+    with pytest.raises(ValueError, match="initial_state must have shape"):
+        call(initial_state=torch.empty(B, H, V, K + 1, device=meta))
+    with pytest.raises(ValueError, match="initial_state must be on"):
+        call(initial_state=torch.empty(B, H, V, K))
+    with pytest.raises(ValueError, match="dt_bias must hold"):
+        call(dt_bias=torch.empty(H * K + 1, device=meta))
+    with pytest.raises(TypeError, match="cu_seqlens must be"):
+        call(cu_seqlens=torch.empty(2, dtype=torch.int64, device=meta))
+    with pytest.raises(ValueError, match="must be contiguous"):
+        call(k=torch.empty(B, T, K, H, dtype=torch.bfloat16, device=meta).transpose(2, 3))
+    with pytest.raises(TypeError, match="v must be"):
+        call(v=torch.empty(B, T, H, V, dtype=torch.float16, device=meta))
+    # all well formed, but not on a GPU: refused, there is no CPU path
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        call()

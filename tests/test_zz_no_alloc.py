@@ -18,7 +18,7 @@ import pytest
 import torch
 
 from chunked_gated_delta_02_gb300.workloads import custom, make_inputs, named
-from kda_testlib import TOL_O_MAXABS, TOL_O_REL, TOL_S_REL, rel_l2, to_dev
+from kda_testlib import TOL_O_MAXABS, TOL_O_REL, TOL_S_REL, assert_parity, oracle_full, rel_l2, to_dev
 
 
 def test_too_large_is_refused_before_any_cuda_call():
@@ -60,6 +60,10 @@ def test_noalloc_matches_kda_fwd_on_two_calls_in_a_row():
         assert np.all(np.isfinite(a)) and np.all(np.isfinite(f_na.cpu().numpy())), name
         assert rel_l2(a, b) <= TOL_O_REL and float(np.max(np.abs(a - b))) <= TOL_O_MAXABS, name
         assert rel_l2(f_na.cpu().numpy(), f_ref.cpu().numpy()) <= TOL_S_REL, name
+        # and against the fp64 oracle directly, so that a fault common to both entry points
+        # (say, in how the scratch is laid out) cannot pass unseen
+        ref_o, ref_f = oracle_full(inp)
+        assert_parity(o_na, f_na, ref_o, ref_f, f"noalloc {name} vs oracle")
 
 
 @pytest.mark.gpu
