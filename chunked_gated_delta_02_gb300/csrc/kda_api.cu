@@ -241,7 +241,7 @@ kda_status_t fill_problem(kda::Problem &p, const Layout &L, void *ws, const void
   const cudaError_t e = once([&](int d) {
     int *a = nullptr;
     const cudaError_t r = cudaGetSymbolAddress(reinterpret_cast<void **>(&a), g_kda_device_status);
-    if (r == cudaSuccess && d < 64) status_addr[d].store(a, std::memory_order_relaxed);
+    if (r == cudaSuccess && d >= 0 && d < 64) status_addr[d].store(a, std::memory_order_relaxed);
     return r;
   });
   p.dev_status = (dev >= 0 && dev < 64) ? status_addr[dev].load(std::memory_order_relaxed) : nullptr;

@@ -43,9 +43,9 @@
 // All block products of A and P come from ONE tensor-core product (tcgen05,
 // tf32 operands, fp32 accumulators in tensor memory), accumulated over two
 // halves of the channels so that the operands fit twice per SM:
-//   D = [k X ; q X] (128 x K)  x  [k Y ; k Ys ; k Ys_0 2^{B_1} ; k Ys_1 2^{B_2} ; k Ys_0 c_30]^T
-// Columns 0-63 give the diagonal blocks, 64-127 the blocks next to the
-// diagonal, 128-175 the three blocks further out. The unit lower triangular
+//   D = [k X ; q X] (128 x K)  x  [k Y ; k Ys_{0..2} ; k Ys_0 2^{B_1} ; k Ys_1 2^{B_2} ; k Ys_0 c_30]^T
+// Columns 0-63 give the diagonal blocks, 64-111 the blocks next to the
+// diagonal, 112-159 the three blocks further out. The unit lower triangular
 // inverse T = (I + A)^{-1} is blocked: the two 32 x 32 diagonal halves by forward
 // substitution in fp32 (one thread per column), then the lower-left 32 x 32 block
 // -T_[23] A_[23][01] T_[01] as two small tensor-core products (fp16 operands, fp32
@@ -60,15 +60,15 @@
 namespace kda {
 
 constexpr int kPrepThreads = 256;
-constexpr int kOpBRows = 176;                 // J-side operand rows
-constexpr uint32_t kPrepTmemCols = 256;       // D_AP: cols 0..175; D_M: cols 192..255
+constexpr int kOpBRows = 160;                 // J-side operand rows
+constexpr uint32_t kPrepTmemCols = 256;       // D_AP: cols 0..159; D_M: cols 192..255
 constexpr long long kPrepWaitLimit = 4000000000LL;
 
 // Shared memory (byte offsets from the 1024-aligned base). The operands hold one half of the
 // channels (64) at a time, as tf32 in 128-byte-swizzled panels of 32 channels.
 struct PrepLayout {
   static constexpr uint32_t opA = 0;                            // [k X ; q X]: 2 panels x 128 rows x 128 B
-  static constexpr uint32_t opB = opA + 2 * 128 * 128;          // J side:      2 panels x 176 rows x 128 B
+  static constexpr uint32_t opB = opA + 2 * 128 * 128;          // J side:      2 panels x 160 rows x 128 B
   static constexpr uint32_t opEnd = opB + 2 * kOpBRows * 128;
   // after the A/P product the operands are dead. In their place: A's two diagonal halves
   // transposed (fp32 [2 x 32][36]), the fp16 operands of the lower-left merge (32 rows of 128-byte
@@ -391,7 +391,7 @@ prep_kernel(const Problem p) {
     } else if (J == 1) {
       x1 = ex2_4(Bm[2]);
     }
-    const int xrow = ((J == 0) ? 128 : 144) + 4 * sbi, yrow = 160 + 4 * sbi;
+    const int xrow = ((J == 0) ? 112 : 128) + 4 * sbi, yrow = 144 + 4 * sbi;
     const float4 kn4 = *reinterpret_cast<const float4 *>(&ms.kn[row0]);   // this thread's four rows
     const float4 qn4 = *reinterpret_cast<const float4 *>(&ms.qn[row0]);
     const float knr[4] = {kn4.x, kn4.y, kn4.z, kn4.w};
@@ -412,7 +412,7 @@ prep_kernel(const Problem p) {
       const F4 ys = mul4(kv[r], suf);
       suf = mul4(suf, al[r]);
       st_tf32x4(opB_at(0, r), mul4(ys, eBinv));
-      st_tf32x4(opB_at(64, r), ys);
+      if (J < 3) st_tf32x4(opB_at(64, r), ys);   // no block lies to the right of the last one
       if (J < 2) st_tf32x4(opB_at(xrow - row0, r), mul4(ys, x1));
       if (J == 0) st_tf32x4(opB_at(yrow - row0, r), mul4(ys, x2));
       st_half4(kt_img + img_off(r), mul4(ys, mul4(SJ, splat4(knr[r]))));
@@ -432,7 +432,7 @@ prep_kernel(const Problem p) {
     }
   }
 
-  // ---- pass 3: read A and P back from TMEM (cols 0..175)
+  // ---- pass 3: read A and P back from TMEM (cols 0..159)
   wait_mma();
   __syncthreads();
   // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (lane = D row): the row blocks {Ilo, Ilo + 1}, with
@@ -451,9 +451,9 @@ prep_kernel(const Problem p) {
     const bool isA = row < 64;
     const float rowf = isA ? ms.beta[row] * ms.kn[row] : ms.qn[row - 64] * p.scale;
     const int thr = isA ? row : row - 63;   // column j is kept when j < thr
-    // D column block of row block I2, block column J2 <= I2: 0-3 the diagonal, 4-7 the blocks next
-    // to it, 8 (2, 0), 9 (3, 1), 10 (3, 0)
-    auto col_block = [](int I2, int J2) { return J2 == I2 ? I2 : J2 == I2 - 1 ? 4 + J2 : (I2 == 2 ? 8 : J2 == 1 ? 9 : 10); };
+    // D column block of row block I2, block column J2 <= I2: 0-3 the diagonal, 4-6 the blocks next
+    // to it, 7 (2, 0), 8 (3, 1), 9 (3, 0)
+    auto col_block = [](int I2, int J2) { return J2 == I2 ? I2 : J2 == I2 - 1 ? 4 + J2 : (I2 == 2 ? 7 : J2 == 1 ? 8 : 9); };
     int Js[2];
     Js[0] = Ilo == 0 ? (warp >> 2) : 2 * (warp >> 2);
     Js[1] = Ilo == 0 ? -1 : 2 * (warp >> 2) + 1;

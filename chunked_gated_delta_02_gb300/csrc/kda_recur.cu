@@ -578,7 +578,7 @@ int device_sm_count() {
   const cudaError_t e = once([&](int dev) {
     int n = 0;
     const cudaError_t r = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (r == cudaSuccess && dev < 64) sm_count[dev].store(n, std::memory_order_relaxed);
+    if (r == cudaSuccess && dev >= 0 && dev < 64) sm_count[dev].store(n, std::memory_order_relaxed);
     sms = n;
     return r;
   });
