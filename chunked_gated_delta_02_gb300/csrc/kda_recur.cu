@@ -192,33 +192,6 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
     umma::mbar_fence_init();
     ms.err = 0;
   }
-  // chain threads: state master S[k][0:BV] (fp32, thread k) and its fp16 operand copy
-  // (element index of S[tid][v0 + v] = st0 + v * stv in either state layout)
-  const int stv = (p.flags & kStateKV) ? 1 : K;
-  float S[BV];
-  if (is_chain && tid < K) {
-    if (MODE == kPlain || (MODE == kSegLocal && seg == 0)) {
-      const long long st0 = state_index(p, s, h, tid, v0);
-#pragma unroll
-      for (int v = 0; v < BV; ++v) S[v] = p.init ? state_load(p, st0 + v * stv) : 0.f;
-    } else if (MODE == kSegLocal) {   // zero value columns, identity transition columns
-#pragma unroll
-      for (int v = 0; v < BV; ++v) S[v] = (trans && tid == v0 - p.V + v) ? 1.f : 0.f;
-    } else {   // the segment's true start state from the combine
-      const float *src = seg_block(p.seg_start, p.V) + (long long)v0 * K + tid;
-#pragma unroll
-      for (int v = 0; v < BV; ++v) S[v] = src[(long long)v * K];
-    }
-#pragma unroll
-    for (int c = 0; c < BV / 8; ++c) {
-      uint4 w;
-      w.x = pack_half2(S[8 * c + 0], S[8 * c + 1]);
-      w.y = pack_half2(S[8 * c + 2], S[8 * c + 3]);
-      w.z = pack_half2(S[8 * c + 4], S[8 * c + 5]);
-      w.w = pack_half2(S[8 * c + 6], S[8 * c + 7]);
-      *reinterpret_cast<uint4 *>(sm + Lay::Sh + umma::sw128_chunk(tid, c)) = w;
-    }
-  }
   // Copies of chunk n, into the buffers of parity n & 1, issued by thread 0 of the sub-group that
   // owns the chunk (hand-off block of its (chunk, head) slot; v by TMA, tokens past T read as
   // zeros, tokens of the next packed sequence are zeroed after arrival):
@@ -255,14 +228,57 @@ recur_tc_kernel(const Problem p, const __grid_constant__ TmaMaps maps) {
       umma::bulk_g2s(kb + Lay::kb_gam, slot_of(n) + hand_off_gam(K), K * 4, &ms.bar_kt[b]);
     }
   };
+  // barriers initialised and the zeroed operands ordered before the first copies, which start at
+  // once: chunk 0 before the initial state is loaded
   umma::fence_proxy_async_smem();
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
-  if (!is_chain && lt == 0 && sg < nch) {
-    stage_in(sg);
-    stage_qt(sg);
-    stage_kt(sg);
+  if (!is_chain && lt == 0 && sg == 0 && nch > 0) {
+    stage_in(0);
+    stage_qt(0);
+    stage_kt(0);
+  }
+  // chain threads: state master S[k][0:BV] (fp32, thread k) and its fp16 operand copy
+  // (element index of S[tid][v0 + v] = st0 + v * stv in either state layout)
+  const int stv = (p.flags & kStateKV) ? 1 : K;
+  float S[BV];
+  if (is_chain && tid < K) {
+    if (MODE == kPlain || (MODE == kSegLocal && seg == 0)) {
+      const long long st0 = state_index(p, s, h, tid, v0);
+#pragma unroll
+      for (int v = 0; v < BV; ++v) S[v] = p.init ? state_load(p, st0 + v * stv) : 0.f;
+    } else if (MODE == kSegLocal) {   // zero value columns, identity transition columns
+#pragma unroll
+      for (int v = 0; v < BV; ++v) S[v] = (trans && tid == v0 - p.V + v) ? 1.f : 0.f;
+    } else {   // the segment's true start state from the combine
+      const float *src = seg_block(p.seg_start, p.V) + (long long)v0 * K + tid;
+#pragma unroll
+      for (int v = 0; v < BV; ++v) S[v] = src[(long long)v * K];
+    }
+#pragma unroll
+    for (int c = 0; c < BV / 8; ++c) {
+      uint4 w;
+      w.x = pack_half2(S[8 * c + 0], S[8 * c + 1]);
+      w.y = pack_half2(S[8 * c + 2], S[8 * c + 3]);
+      w.z = pack_half2(S[8 * c + 4], S[8 * c + 5]);
+      w.w = pack_half2(S[8 * c + 6], S[8 * c + 7]);
+      *reinterpret_cast<uint4 *>(sm + Lay::Sh + umma::sw128_chunk(tid, c)) = w;
+    }
+  }
+  umma::fence_proxy_async_smem();
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  // chunk 1 once chunk 0's inputs have landed, so that the first chunk has the memory to itself
+  if (!is_chain && lt == 0 && sg == 1 && nch > 1) {
+    if (umma::mbar_wait_bounded(&ms.bar_in[0], 0, kWaitLimit)) {
+      stage_in(1);
+      stage_qt(1);
+      stage_kt(1);
+    } else {
+      atomicExch(&ms.err, 1);
+    }
   }
   const uint32_t tmem = ms.tmem_slot;
   const uint32_t tD3 = tmem + Tm::d3;
