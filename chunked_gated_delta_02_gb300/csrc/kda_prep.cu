@@ -438,8 +438,9 @@ prep_kernel(const Problem p) {
   // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (lane = D row): the row blocks {Ilo, Ilo + 1}, with
   // Ilo = 0 (quadrants 0, 2) or 2 (quadrants 1, 3), one per half-warp. Each step of a warp handles
   // one block column J for both row blocks at once: it loads the D column block of (Ilo, J) and of
-  // (Ilo + 1, J) and each half-warp keeps its own. The two warps of a quadrant split the J: J = 0
-  // and 1 (none) for the first warp of an upper (lower) quadrant, J = 2 and 3 (1) for the second.
+  // (Ilo + 1, J) and each half-warp keeps its own. The two warps of a quadrant split the J values
+  // (below) so that warps 0 and 1, which then solve the two diagonal halves, write every diagonal
+  // block of -A they read themselves.
   // A rows (< 64) go to fp32 matAt (blocks of the diagonal halves, negated and transposed) or to
   // the fp16 operand of the lower-left merge (the lower-left quarter), times
   // beta_i |k_i|^-1 |k_j|^-1, strictly lower; P rows to the [-I ; P] operand (times
@@ -455,8 +456,11 @@ prep_kernel(const Problem p) {
     // to it, 7 (2, 0), 8 (3, 1), 9 (3, 0)
     auto col_block = [](int I2, int J2) { return J2 == I2 ? I2 : J2 == I2 - 1 ? 4 + J2 : (I2 == 2 ? 7 : J2 == 1 ? 8 : 9); };
     int Js[2];
-    Js[0] = Ilo == 0 ? (warp >> 2) : 2 * (warp >> 2);
-    Js[1] = Ilo == 0 ? -1 : 2 * (warp >> 2) + 1;
+    // upper quadrants (row blocks 0, 1): the first warp takes both block columns, the second none;
+    // lower quadrants (row blocks 2, 3): the first warp the diagonal columns 2, 3, the second 0, 1.
+    // So warps 0 and 1 write every diagonal block of -A that their substitution reads.
+    Js[0] = Ilo == 0 ? ((warp >> 2) ? -1 : 0) : ((warp >> 2) ? 0 : 2);
+    Js[1] = Ilo == 0 ? ((warp >> 2) ? -1 : 1) : ((warp >> 2) ? 1 : 3);
     float xlo[2][16], xhi[2][16];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -508,6 +512,9 @@ prep_kernel(const Problem p) {
       }
     }
   }
+  // The diagonal blocks of -A that the substitution reads (matAt) were written by the same warp
+  // (warp 0 the upper half, warp 1 the lower one): the lanes of that warp meet here.
+  if (warp < 2) __syncwarp();
   // Tb^T operand (row j, column m: T[m][j] beta_j, fp16): the 16-byte chunk of (row j, columns
   // 8 c8 .. 8 c8 + 7)
   auto opT_chunk = [&](int j, int c8) -> unsigned char * { return sm + Lay::opT + umma::sw128_chunk(j, c8); };
