@@ -295,3 +295,11 @@ def test_deterministic_at_full_size():
         outs.append((o, fs))
     for o, fs in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(fs, outs[0][1])
+
+
+def test_varlen_past_the_schedule_bins():
+    """A packed batch of more than 8192 chunks (T > 524k tokens) is past the schedule's counting-
+    sort bins: the sequences then run in input order instead of longest first. The results are the
+    same; every output is compared with the oracle."""
+    w = custom(H=1, K=64, V=64, seqlens=[300000, 100, 200000, 30000], init_state=True, lower_bound=-0.2)
+    check_full(make_inputs(w, seed=71), "varlen beyond the bins")
