@@ -303,3 +303,21 @@ def test_varlen_past_the_schedule_bins():
     same; every output is compared with the oracle."""
     w = custom(H=1, K=64, V=64, seqlens=[300000, 100, 200000, 30000], init_state=True, lower_bound=-0.2)
     check_full(make_inputs(w, seed=71), "varlen beyond the bins")
+
+
+# Fixed-length batches with more 64-column (sequence, head, V slice) CTAs than SMs, so that the
+# recurrence runs in several waves: short sequences, a ragged last chunk, with and without initial
+# states, both head dimensions.
+WAVE_SHAPES = [
+    (10, 200, 16, 128, 128, -0.5, True), (20, 50, 16, 128, 128, -5.0, True),
+    (20, 100, 16, 64, 64, -1.0, False), (12, 129, 16, 128, 64, -0.2, True),
+]
+
+
+@pytest.mark.parametrize("B,T,H,K,V,lb,init", WAVE_SHAPES)
+def test_multi_wave_shapes(B, T, H, K, V, lb, init):
+    import chunked_gated_delta_02_gb300 as kda
+    assert B * H * (V // 64) > 152            # more jobs than the SMs of a GB300
+    w = custom(B=B, T=T, H=H, K=K, V=V, lower_bound=lb, init_state=init)
+    check_full(make_inputs(w, seed=B * 7 + T), f"multi-wave B{B}-T{T}-H{H}-K{K}-V{V}")
+    assert kda.device_status() == 0
