@@ -52,6 +52,7 @@
 // accumulators): Z = A_[23][01] T_[01], then (T_[23] Z)^T = Z^T T_[23]^T. All of T lands, scaled as
 // Tb = T diag(beta), in the fp16 operand of M = [-I ; P] Tb, a third tensor-core
 // product (128 x 64 x 64).
+#include <cstddef>
 #include <type_traits>
 
 #include "kda_common.cuh"
@@ -97,11 +98,15 @@ struct PrepMisc {
   uint64_t bar;
   uint32_t tmem_slot;
   int err;
-  float beta[kChunk], kn[kChunk], qn[kChunk];
+  // 16-byte aligned: the norms are read four rows at a time
+  alignas(16) float beta[kChunk];
+  alignas(16) float kn[kChunk];
+  alignas(16) float qn[kChunk];
   // per (4-row sub-block j, channel quad): the sum of la2 over the sub-block, then, in place, the
   // exclusive prefix over the sub-blocks (E[j] = sum over rows < 4 j; E[16] = the whole chunk)
   float4 epre[17][16];
 };
+static_assert(offsetof(PrepMisc, kn) % 16 == 0 && offsetof(PrepMisc, qn) % 16 == 0, "float4 reads of the norms");
 
 __device__ __forceinline__ uint32_t ldg_u32(const __nv_bfloat16 *p) {
   return __ldg(reinterpret_cast<const unsigned int *>(p));
