@@ -336,8 +336,10 @@ prep_kernel(const Problem p) {
       // per head: the token's gate (low half of rawg[r].x) in every channel
       const F4 g4 = per_head ? splat4(__uint_as_float(rawg[r].x << 16)) : bf4_to_f4(rawg[r]);
       const F4 e = {__ffma2_rn(make_float2(cg, cg), g4.lo, cdt.lo), __ffma2_rn(make_float2(cg, cg), g4.hi, cdt.hi)};
-      la[r] = {make_float2(lbl2 * rcp_approx(1.f + ex2_approx(e.lo.x)), lbl2 * rcp_approx(1.f + ex2_approx(e.lo.y))),
-               make_float2(lbl2 * rcp_approx(1.f + ex2_approx(e.hi.x)), lbl2 * rcp_approx(1.f + ex2_approx(e.hi.y)))};
+      // la = lb log2(e) / (1 + 2^e), the additions and multiplications as packed pairs
+      const F4 d = add4(ex2_4(e), splat4(1.f));
+      la[r] = mul4(splat4(lbl2), {make_float2(rcp_approx(d.lo.x), rcp_approx(d.lo.y)),
+                                  make_float2(rcp_approx(d.hi.x), rcp_approx(d.hi.y))});
       kv[r] = bf4_to_f4(rawk[r]);
       qv[r] = bf4_to_f4(rawq[r]);
     }
