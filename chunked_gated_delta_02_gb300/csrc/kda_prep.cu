@@ -266,19 +266,22 @@ prep_kernel(const Problem p) {
 #pragma unroll
     for (int r = 0; r < 8; ++r) red[r] = 0.f;
     if (nrows > 0) {
+      float2 acc[8];   // the same sums as two packed partial sums (even and odd channels)
+#pragma unroll
+      for (int r = 0; r < 8; ++r) acc[r] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int hf = 0; hf < K / 64; ++hf) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const F4 kv = bf4_to_f4(rk[hf][r]), qv = bf4_to_f4(rq[hf][r]);
-          red[r] = fmaf(kv.lo.x, kv.lo.x, fmaf(kv.lo.y, kv.lo.y, fmaf(kv.hi.x, kv.hi.x, fmaf(kv.hi.y, kv.hi.y, red[r]))));
-          red[4 + r] =
-              fmaf(qv.lo.x, qv.lo.x, fmaf(qv.lo.y, qv.lo.y, fmaf(qv.hi.x, qv.hi.x, fmaf(qv.hi.y, qv.hi.y, red[4 + r]))));
+          acc[r] = __ffma2_rn(kv.hi, kv.hi, __ffma2_rn(kv.lo, kv.lo, acc[r]));
+          acc[4 + r] = __ffma2_rn(qv.hi, qv.hi, __ffma2_rn(qv.lo, qv.lo, acc[4 + r]));
         }
       }
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        if (r >= nrows) red[r] = red[4 + r] = 0.f;
+        red[r] = r < nrows ? acc[r].x + acc[r].y : 0.f;
+        red[4 + r] = r < nrows ? acc[4 + r].x + acc[4 + r].y : 0.f;
       }
     }
     // reduce-scatter of the 8 row sums over the 16 lanes of this sub-block: after the four steps
@@ -506,10 +509,12 @@ prep_kernel(const Problem p) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float4 knj = *reinterpret_cast<const float4 *>(&ms.kn[16 * Jb + 4 * q]);
-          const float kj[4] = {knj.x, knj.y, knj.z, knj.w};
+          const float2 nr2 = make_float2(nrowf, nrowf);
+          const float2 y01 = __fmul2_rn(make_float2(x[4 * q], x[4 * q + 1]), __fmul2_rn(nr2, make_float2(knj.x, knj.y)));
+          const float2 y23 = __fmul2_rn(make_float2(x[4 * q + 2], x[4 * q + 3]), __fmul2_rn(nr2, make_float2(knj.z, knj.w)));
+          const float y[4] = {y01.x, y01.y, y23.x, y23.y};
 #pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2)
-            atc[(4 * q + e2) * Lay::LDQ] = (16 * Jb + 4 * q + e2 < thr) ? x[4 * q + e2] * nrowf * kj[e2] : 0.f;
+          for (int e2 = 0; e2 < 4; ++e2) atc[(4 * q + e2) * Lay::LDQ] = (16 * Jb + 4 * q + e2 < thr) ? y[e2] : 0.f;
         }
         continue;
       }
@@ -519,10 +524,12 @@ prep_kernel(const Problem p) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float4 knj = *reinterpret_cast<const float4 *>(&ms.kn[16 * Jb + 4 * q]);
-        const float kj[4] = {knj.x, knj.y, knj.z, knj.w};
-        float y[4];
+        const float2 r2 = make_float2(rowf, rowf);
+        const float2 y01 = __fmul2_rn(make_float2(x[4 * q], x[4 * q + 1]), __fmul2_rn(r2, make_float2(knj.x, knj.y)));
+        const float2 y23 = __fmul2_rn(make_float2(x[4 * q + 2], x[4 * q + 3]), __fmul2_rn(r2, make_float2(knj.z, knj.w)));
+        float y[4] = {y01.x, y01.y, y23.x, y23.y};
 #pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) y[e2] = (16 * Jb + 4 * q + e2 < thr) ? x[4 * q + e2] * rowf * kj[e2] : 0.f;
+        for (int e2 = 0; e2 < 4; ++e2) y[e2] = (16 * Jb + 4 * q + e2 < thr) ? y[e2] : 0.f;
         const uint32_t cc = (uint32_t)(2 * Jb + (q >> 1));
         *reinterpret_cast<uint2 *>(rowp + (((cc ^ (uint32_t)(row & 7)) << 4) | ((uint32_t)(q & 1) << 3))) =
             make_uint2(pack_h2(y[0], y[1]), pack_h2(y[2], y[3]));
