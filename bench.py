@@ -60,6 +60,9 @@ def parse():
                     help="context parallelism: auto (the library's plan), off, or a segment count")
     ap.add_argument("--heads", type=int, default=None,
                     help="override the workload's head count (same shapes and distributions otherwise)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override a fixed-length workload's batch size (a smaller case of the same "
+                         "shape, e.g. for an ncu capture)")
     return ap.parse_args()
 
 
@@ -76,6 +79,11 @@ def workload_of(args):
     from dataclasses import replace
     from chunked_gated_delta_02_gb300.workloads import named
     w = named(args.workload)
+    batch = getattr(args, "batch", None)
+    if batch:
+        if w.is_varlen:
+            raise SystemExit("--batch applies to fixed-length workloads")
+        w = replace(w, B=batch)
     heads = getattr(args, "heads", None)
     return replace(w, H=heads) if heads else w
 
@@ -402,7 +410,8 @@ def run_ours(args):
         abytes = algorithmic_bytes(inp)
         path_gbs = abytes / (ms * 1e-3) / 1e9
         # the committed ncu traffic is per named workload in its default plan
-        traffic_key = args.workload if (not args.heads and n_seg < 2) else f"{args.workload}-H{H}-cp{n_seg}"
+        resized = bool(args.heads or getattr(args, "batch", None))
+        traffic_key = args.workload if (not resized and n_seg < 2) else f"{args.workload}-B{B}-H{H}-cp{n_seg}"
         roofs = kernel_rooflines(inp, ms_prep, ms_rec, peak, peak_src, traffic_key)
         if n_seg >= 2:
             roofs = [dict(r, kernel="recurrence (K2: local pass, combine, final pass)")

@@ -113,3 +113,14 @@ def test_each_kernel_is_credited_with_its_own_bytes():
     assert abs(roofs[0]["frac"] - th * 770 / 90.7e-6 / 1e9 / 6680.8) < 1e-9
     assert abs(roofs[0]["frac"] - 0.1666) < 1e-3
     assert roofs[0]["traffic"] is None and roofs[0]["traffic_over_algorithmic"] is None
+
+
+def test_batch_and_head_overrides(monkeypatch):
+    """--batch and --heads resize a fixed-length workload and keep everything else; a varlen
+    workload refuses --batch."""
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", "large_batch", "--batch", "16", "--heads", "8"])
+    w = bench.workload_of(bench.parse())
+    assert (w.B, w.T, w.H, w.K, w.V, w.lower_bound) == (16, 512, 8, 128, 128, -5.0)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", "varlen", "--batch", "16"])
+    with pytest.raises(SystemExit):
+        bench.workload_of(bench.parse())
