@@ -310,7 +310,7 @@ prep_kernel(const Problem p) {
   unsigned char *hb = p.hand + slot * p.hand_stride;
   unsigned char *kg_img = hb + hand_off_kg(K), *kt_img = hb + hand_off_kt(K), *qt_img = hb + hand_off_qt(K);
 
-#pragma unroll 1
+#pragma unroll   // two channel halves: unrolled, the second half's gate work can overlap the first half's stores
   for (int hf = 0; hf < K / 64; ++hf) {
     // ---- pass 2a: gate and log decay of 4 rows x 4 channels (k and q as loaded by pass 1). With
     // one gate per token and head (kGatePerHead) g is [B,T,H]: its element index is the token
