@@ -82,7 +82,7 @@ struct PrepLayout {
   static constexpr uint32_t opZ = 22 * 1024;                    // Z^T, MN-major      (A of Z^T T_[23]^T)
   static constexpr uint32_t opT = 26 * 1024;                    // Tb^T:      64 rows x 128 B (fp16)
   static constexpr uint32_t opM = 34 * 1024;                    // [-I ; P]: 128 rows x 128 B (fp16)
-  static constexpr uint32_t mstage = 0;                         // M, staged for its bulk copy: 128 rows x 128 B
+  static constexpr uint32_t mstage = 0;                         // M, staged for its copy-out: 128 rows x 128 B
   static constexpr uint32_t end = (opM + 128 * 128 > opEnd) ? opM + 128 * 128 : opEnd;
   static_assert(matAt + 64 * LDQ * 4 <= opAll, "transposed A overlaps the merge operands");
   static_assert(opT + 64 * 128 <= opM, "Tb^T operand overlaps the [-I ; P] operand");
@@ -676,8 +676,8 @@ prep_kernel(const Problem p) {
   }
   wait_mma();
   // output: row r of M (TMEM lane r) -> fp16 row r in the swizzled chunk order r*8 + (cc ^ (r & 7)),
-  // staged in shared memory (the operands are dead) and written to the hand-off block with one
-  // bulk copy; warp w takes lanes 32 (w % 4) .. + 31 and columns 32 (w / 4) .. + 31
+  // staged in shared memory (the operands are dead), then copied to the hand-off block with
+  // coalesced 16-byte stores; warp w takes lanes 32 (w % 4) .. + 31 and columns 32 (w / 4) .. + 31
   {
     const int r = 32 * (warp & 3) + lane;
     uint4 *stage = reinterpret_cast<uint4 *>(sm + Lay::mstage) + r * 8;
@@ -693,17 +693,16 @@ prep_kernel(const Problem p) {
                        pack_h2(x[8 * hc + 4], x[8 * hc + 5]), pack_h2(x[8 * hc + 6], x[8 * hc + 7]));
     }
   }
-  umma::fence_proxy_async_smem();   // the staged rows to the bulk copy
   umma::fence_before_sync();
   __syncthreads();
-  if (tid == 0) {
-    if (ms.err) {
-      atomicExch(p.dev_status, kDevWaitTimeout);
-    } else {
-      umma::bulk_s2g(p.mats + slot * p.mat_stride, sm + Lay::mstage, 128 * 128);
-      umma::bulk_commit();
-      umma::bulk_wait_read();   // the staging copy stays valid until it has been read
-    }
+  if (tid == 0 && ms.err) atomicExch(p.dev_status, kDevWaitTimeout);
+  // the staged 16 KB to the hand-off block: eight threads per 128-byte row, 16 bytes each, four
+  // rows per thread (every load and store a whole line per eight lanes)
+  {
+    const uint4 *src = reinterpret_cast<const uint4 *>(sm + Lay::mstage);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.mats + slot * p.mat_stride);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[tid + kPrepThreads * i] = src[tid + kPrepThreads * i];
   }
   if (warp == 0) umma::tmem_dealloc(tmem, kPrepTmemCols);
 }
